@@ -1,0 +1,388 @@
+"""Throughput of the attention forward on one GB300 (or N replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME]
+
+One step is one fa_fwd call (the whole hot path) over one batch of the
+workload's synthetic inputs, already resident in device memory. Rank 0 prints
+one JSON line. With N > 1 (torchrun, one rank per GPU) every rank runs its
+own replica of the workload (weak scaling; the path needs no collective), and
+the timed region is bracketed by barriers; the max time over ranks is used.
+
+--impl reference times the fp64 CPU oracle instead (bounded row samples of the
+same workload per step) on the host cores, on rank 0 only.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from exact_attention_16_gb300 import metrics  # noqa: E402
+from exact_attention_16_gb300.workloads import WORKLOADS, by_name, draw_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "causal_gqa8_b1_s16384"
+L2_BYTES = 129 * 1000 * 1000
+METRIC = "attention fwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 tensor peak"
+KERNEL_SOURCES = ["exact_attention_16_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_16_gb300/csrc/ptx_sm103.cuh"]
+TRAFFIC_SUMMARY = "profiles/fa_fwd_kernel_traffic.md"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d["bf16_tflops"], "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload (else None)."""
+    path = os.path.join(ROOT, TRAFFIC_SUMMARY)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha") != kernel_source_hash() or fields.get("workload") != workload:
+        return None
+    try:
+        return int(float(fields["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.4)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                clk, cmax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            sm.append(clk)
+            mx = cmax
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_ours(args, w):
+    import torch
+
+    from exact_attention_16_gb300 import api
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = dist_mod
+    dev = torch.device("cuda", local)
+    q, k, v = draw_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.fa_fwd(qd, kd, vd, scale=w.scale, causal=w.causal, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    if api.fa_status() != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    flop = metrics.flops(w.B, w.Sq, w.Sk, w.Hq, w.D, w.causal)
+    in_bytes = sum(x.numel() * x.element_size() for x in (q, k, v))
+    # Inputs larger than L2 are timed back to back. Smaller ones get an L2
+    # flush (a 256 MiB write) before every launch, and the step time is then
+    # the sum of the per-launch event intervals, which exclude the flush.
+    flush = None if in_bytes > L2_BYTES else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    l2_note = (f"inputs larger than L2 (q+k+v = {in_bytes >> 20} MiB > 129 MB); no flush" if flush is None
+               else f"inputs ({in_bytes >> 20} MiB) smaller than L2: 256 MiB L2 flush before each launch, "
+                    "flush excluded from the per-launch event timing")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    if api.fa_status() != 0:
+        raise RuntimeError("device status not OK after the timed region")
+    launch_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    total_ms = starts[0].elapsed_time(ends[-1]) if flush is None else sum(launch_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the same public call with pinned host buffers:
+    # H2D of q, k, v, the kernel, and D2H of O and LSE every step
+    hq_, hk_, hv_ = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        qd.copy_(hq_, non_blocking=True)
+        kd.copy_(hk_, non_blocking=True)
+        vd.copy_(hv_, non_blocking=True)
+        api.fa_fwd(qd, kd, vd, scale=w.scale, causal=w.causal, out=out, lse=lse)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = in_bytes
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    peaks = measured_peaks()
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    achieved = flop / (avg_launch_ms * 1e-3) / 1e12
+    value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded PCG64 normal draws rounded to the dtype)",
+        "config": {
+            "workload": w.name, "B": w.B, "Sq": w.Sq, "Sk": w.Sk, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+            "causal": w.causal, "scale": w.scale, "flops_per_step": flop,
+            "l2": l2_note,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "pct_of_peak": round(100.0 * (value / world) / peaks["bf16_tflops"], 2),
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "peak_source": peaks["source"] + " bf16 burst",
+            "traffic": recorded_traffic(w.name),
+            "algorithmic_bytes": metrics.algorithmic_bytes(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D),
+            "kernel": "fa_fwd_kernel",
+            "avg_launch_ms": round(avg_launch_ms, 4),
+        },
+        "e2e": {
+            "value": round(world * flop * e2e_steps / e2e_s / 1e12, 2),
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, q, k, v, budget_s=args.cpu_budget)
+    if dist:
+        dist.destroy_process_group()
+    return rank, result
+
+
+def oracle_sample(w, q32, k32, v32, rows_per_head: int, n_heads: int):
+    """Time the oracle on the last `rows_per_head` rows of the first heads;
+    returns (seconds, flops done)."""
+    import oracle
+
+    flop = 0
+    t0 = time.perf_counter()
+    for idx in range(n_heads):
+        b, hq = divmod(idx % (w.B * w.Hq), w.Hq)
+        rows = np.arange(max(0, w.Sq - rows_per_head), w.Sq)
+        oracle.attention_rows(q32, k32, v32, w.scale, w.causal, b, hq, rows)
+        flop += 4 * w.D * sum(metrics.visible_keys(int(i), w.Sq, w.Sk, w.causal) for i in rows)
+    return time.perf_counter() - t0, flop
+
+
+def cpu_baseline(w, q, k, v, budget_s: float):
+    q32, k32, v32 = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    rows = min(w.Sq, 256)
+    heads = 1
+    secs, flop = oracle_sample(w, q32, k32, v32, rows, heads)
+    # grow the sample until it takes about `budget_s`
+    while secs < budget_s * 0.5 and heads < 4 * w.B * w.Hq:
+        heads *= 2
+        secs, flop = oracle_sample(w, q32, k32, v32, rows, heads)
+    return {
+        "value": round(flop / secs / 1e12, 6),
+        "unit": "TFLOP/s",
+        "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1)),
+        "kind": "oracle",
+        "sample": f"fp64 NumPy two-pass oracle on the last {rows} query rows of {heads} (batch, head) pairs "
+                  f"of {w.name} ({secs:.1f} s; BLAS threads = cores, elementwise NumPy single-threaded)",
+    }
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return rank, None
+    q, k, v = draw_inputs(w)
+    q32, k32, v32 = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    # size one step so that warm-up + timed steps take about two minutes
+    per_step_s = max(0.05, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows = 16
+    secs, _ = oracle_sample(w, q32, k32, v32, rows, 1)
+    while secs < per_step_s * 0.5 and rows < w.Sq:
+        rows = min(w.Sq, rows * 2)
+        secs, _ = oracle_sample(w, q32, k32, v32, rows, 1)
+    for _ in range(args.warmup):
+        oracle_sample(w, q32, k32, v32, rows, 1)
+    t_total, f_total = 0.0, 0
+    for _ in range(args.steps):
+        s, f = oracle_sample(w, q32, k32, v32, rows, 1)
+        t_total += s
+        f_total += f
+    value = f_total / t_total / 1e12
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    sample = f"fp64 NumPy two-pass oracle, last {rows} query rows of (b=0, h=0) of {w.name} per step"
+    return rank, {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t_total / max(1, args.steps), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded PCG64 normal draws rounded to the dtype)",
+        "config": {"workload": w.name, "B": w.B, "Sq": w.Sq, "Sk": w.Sk, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[x.name for x in WORKLOADS])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = by_name(args.workload)
+    if args.impl == "reference":
+        rank, res = run_reference(args, w)
+    else:
+        rank, res = run_ours(args, w)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

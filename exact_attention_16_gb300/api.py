@@ -1,0 +1,161 @@
+"""Python binding of the C ABI in include/fa.h (ctypes; marshalling only).
+
+Every function here has the name of the C entry point it wraps. Tensors are
+PyTorch CUDA tensors; the binding checks dtype, device, shape and contiguity,
+passes raw device pointers and the current CUDA stream, and raises
+:class:`FAError` on a non-zero status. There is no fallback: if the compiled
+library is missing, loading it raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "FAError",
+    "lib",
+    "library_path",
+    "fa_fwd",
+    "fa_status",
+    "fa_status_string",
+    "fa_version",
+    "fa_debug_set_fault",
+    "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libfa_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_DTYPE_FP16, FA_DTYPE_BF16 = 0, 1
+
+# name -> (restype, argtypes); the entry points include/fa.h declares
+EXPORTED_SYMBOLS = {
+    "fa_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_void_p]),
+    "fa_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fa_version": (ctypes.c_int, []),
+    "fa_debug_set_fault": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        name = lib().fa_status_string(code).decode() if _lib is not None else str(code)
+        super().__init__(f"{what}: {name}" if what else name)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(_LIB_PATH):
+                    raise ImportError(
+                        f"{_LIB_PATH} is missing: build it with `python -m exact_attention_16_gb300.build`")
+                handle = ctypes.CDLL(_LIB_PATH)
+                for name, (res, args) in EXPORTED_SYMBOLS.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float16:
+        return FA_DTYPE_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected torch.bfloat16 or torch.float16")
+
+
+def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=True, stream=None):
+    """Attention forward: returns (O, LSE) (LSE is None if return_lse is False
+    and no ``lse`` buffer is given).
+
+    q: (B, Sq, Hq, D); k, v: (B, Sk, Hkv, D); all contiguous CUDA tensors of
+    one 16-bit dtype on one device. ``scale`` defaults to 1/sqrt(D). ``causal``
+    selects the bottom-right aligned mask (query i sees key j iff
+    j <= i + Sk - Sq). ``out`` / ``lse`` may be preallocated (B, Sq, Hq, D)
+    and (B, Hq, Sq) float32 tensors.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D (batch, seq, heads, head_dim)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must be on one device")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError("k and v must be (B, Sk, Hkv, D) matching q")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    elif lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32
+                              or lse.device != q.device or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 (B, Hq, Sq) tensor on q's device")
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else None,
+                          B, Sq, Sk, Hq, Hkv, D, float(scale), int(bool(causal)), code,
+                          _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd")
+    return out, lse
+
+
+def fa_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word."""
+    return int(lib().fa_status(_stream_handle(stream)))
+
+
+def fa_status_string(code: int) -> str:
+    return lib().fa_status_string(int(code)).decode()
+
+
+def fa_version() -> int:
+    return int(lib().fa_version())
+
+
+def fa_debug_set_fault(skip_load: int, timeout_ms: int = 0) -> int:
+    """Test hook: drop K/V load ``skip_load`` of every CTA (-1 = off)."""
+    return int(lib().fa_debug_set_fault(int(skip_load), int(timeout_ms)))

@@ -1,0 +1,223 @@
+// Host side of the C ABI declared in include/fa.h: argument validation, TMA
+// tensor-map encoding, persistent-grid sizing and the launch on the caller's
+// stream. Every step of the attention itself runs in fa_fwd_kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+__device__ int g_fa_status = 0;
+
+// Sk == 0: no key is visible, so O = 0 and LSE = -inf for every row.
+__global__ void fa_fill_empty_kernel(uint4* o, long long o_vec, float* lse, long long n_lse) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < o_vec; i += stride)
+    o[i] = make_uint4(0, 0, 0, 0);
+  if (lse)
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_lse; i += stride)
+      lse[i] = -__int_as_float(0x7f800000);
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t init_err = cudaSuccess;
+  int num_sms = 0;
+  int* status = nullptr;  // address of g_fa_status on this device
+};
+DeviceState g_dev[kMaxDevices];
+
+std::atomic<int> g_fault_skip_load{-1};
+std::atomic<int> g_fault_timeout_ms{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+template <int D, bool BF16>
+cudaError_t set_smem_attr() {
+  static std::once_flag f[kMaxDevices];
+  static cudaError_t err[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::call_once(f[dev], [&] {
+    err[dev] = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    fa::Smem<D>::kAlloc);
+  });
+  return err[dev];
+}
+
+DeviceState* device_state(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceState& s = g_dev[dev];
+  std::call_once(s.once, [&] {
+    s.init_err = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (s.init_err == cudaSuccess)
+      s.init_err = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.status), g_fa_status);
+  });
+  if (dev_out) *dev_out = dev;
+  return s.init_err == cudaSuccess ? &s : nullptr;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 4-D map over a (B, S, H, D) tensor: dims innermost first (D, H, S, B); the
+// box is 64 elements (128 bytes) x 1 head x 128 rows x 1 batch, 128-byte
+// swizzle, zero fill outside the tensor.
+bool encode_bshd(CUtensorMap* map, const void* ptr, bool bf16, int B, int S, int H, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(S) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+unsigned long long wait_timeout_ns() {
+  const int fault_ms = g_fault_timeout_ms.load();
+  if (fault_ms > 0) return static_cast<unsigned long long>(fault_ms) * 1000000ull;
+  static const unsigned long long env_ns = [] {
+    const char* e = std::getenv("FA_WAIT_TIMEOUT_MS");
+    long long ms = e ? std::atoll(e) : 0;
+    return static_cast<unsigned long long>(ms > 0 ? ms : 2000) * 1000000ull;
+  }();
+  return env_ns;
+}
+
+template <int D, bool BF16>
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::FwdParams& p, int grid,
+           cudaStream_t stream) {
+  if (set_smem_attr<D, BF16>() != cudaSuccess) return FA_ERR_CUDA;
+  fa::fa_fwd_kernel<D, BF16><<<grid, fa::kThreads, fa::Smem<D>::kAlloc, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
+                      int Hq, int Hkv, int D, float scale, int causal, int dtype, fa_stream_t stream_) {
+  // ---- validation (nothing is enqueued on failure)
+  if (B < 0 || Sq < 0 || Sk < 0 || Hq < 0 || Hkv < 0 || D < 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (!q || !o || (Sk > 0 && (!k || !v))) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))) ||
+      (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  // the largest byte stride a tensor map may carry is below 2^40
+  const double q_bytes = static_cast<double>(Sq) * Hq * D * 2, kv_bytes = static_cast<double>(Sk) * Hkv * D * 2;
+  if (q_bytes >= 1099511627776.0 || kv_bytes >= 1099511627776.0) return FA_ERR_UNSUPPORTED;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  DeviceState* ds = device_state(nullptr);
+  if (!ds) return FA_ERR_CUDA;
+
+  if (Sk == 0) {
+    const long long o_vec = static_cast<long long>(B) * Sq * Hq * D * 2 / 16;
+    const long long n_lse = static_cast<long long>(B) * Hq * Sq;
+    fa_fill_empty_kernel<<<ds->num_sms * 4, 256, 0, stream>>>(static_cast<uint4*>(o), o_vec, lse, n_lse);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  fa::FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = Hq / Hkv;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.n_mtiles = (Sq + fa::kBM - 1) / fa::kBM;
+  p.n_kv_tiles = (Sk + fa::kBN - 1) / fa::kBN;
+  p.pair_heads = (p.group % 2 == 0) ? 1 : 0;
+  p.n_units = p.pair_heads ? Hq / 2 : Hq;
+  p.n_mslots = p.pair_heads ? p.n_mtiles : (p.n_mtiles + 1) / 2;
+  const long long items = static_cast<long long>(B) * p.n_units * p.n_mslots;
+  if (items > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  p.n_items = static_cast<int>(items);
+  p.timeout_ns = wait_timeout_ns();
+  p.inject_skip_load = g_fault_skip_load.load();
+  p.status = ds->status;
+
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bshd(&tq, q, bf16, B, Sq, Hq, D) || !encode_bshd(&tk, k, bf16, B, Sk, Hkv, D) ||
+      !encode_bshd(&tv, v, bf16, B, Sk, Hkv, D))
+    return FA_ERR_CUDA;
+
+  const int grid = static_cast<int>(std::min<long long>(items, ds->num_sms));
+  if (D == 128) {
+    return bf16 ? launch<128, true>(tq, tk, tv, p, grid, stream) : launch<128, false>(tq, tk, tv, p, grid, stream);
+  }
+  return bf16 ? launch<64, true>(tq, tk, tv, p, grid, stream) : launch<64, false>(tq, tk, tv, p, grid, stream);
+}
+
+extern "C" int fa_status(fa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* ds = device_state(nullptr);
+  if (!ds) return FA_ERR_CUDA;
+  int value = 0, zero = 0;
+  if (cudaMemcpy(&value, ds->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  return value;
+}
+
+extern "C" const char* fa_status_string(int code) {
+  switch (code) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int fa_version(void) { return 100; }
+
+extern "C" int fa_debug_set_fault(int skip_load, int timeout_ms) {
+  if (skip_load < -1) return FA_ERR_INVALID_ARG;
+  g_fault_skip_load.store(skip_load);
+  g_fault_timeout_ms.store(skip_load >= 0 ? timeout_ms : 0);
+  return FA_OK;
+}

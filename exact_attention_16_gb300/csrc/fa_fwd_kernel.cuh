@@ -1,0 +1,537 @@
+// FlashAttention forward for sm_103a: TMA + mbarrier pipeline, tcgen05 MMAs
+// accumulating in tensor memory, warp-specialised online softmax, causal tile
+// skipping and a persistent longest-first scheduler.
+//
+// What it computes (exact attention, tile by tile with online softmax):
+//   "MiniPaged-Qwen: Qwen3 Prefill FlashAttention", sections 3.1 and 4 (tile
+//   recurrence m, l, alpha, O~, then O = O~ / l), section 6 (GQA head map),
+//   section 13 (bottom-right causal limit); "NVIDIA闪存注意力实操" sections
+//   "在线Softmax算法" (exp2 with log2(e) folded into the scale), "K循环拆分"
+//   (only diagonal tiles are masked, tiles above it are skipped) and
+//   "ProgramId重映射" (longest work first).
+//
+// One CTA per SM loops over work items. A work item is two 128-row query
+// tiles that read the same keys and values: two heads of one GQA group at the
+// same rows when the group size is even, else two consecutive row tiles of one
+// head. Warp roles (320 threads):
+//   warps 0-3  softmax + epilogue for query tile 0 (TMEM lanes 0..127)
+//   warps 4-7  softmax + epilogue for query tile 1
+//   warp  8    TMA producer (Q tiles, then K_j / V_j tiles into a ring)
+//   warp  9    MMA issuer (one thread) and TMEM owner
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// The softmax writes P (16-bit, two per column) over the first 64 columns of
+// its S region; the PV MMA reads P from TMEM and V from shared memory.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;          // query rows per tile (MMA M)
+constexpr int kBN = 128;          // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
+
+enum : int { kStatusOk = 0, kStatusTimeout = 4 };
+
+struct FwdParams {
+  void* o;               // (B, Sq, Hq, D) 16-bit
+  float* lse;            // (B, Hq, Sq) fp32 natural log, may be null
+  int B, Sq, Sk, Hq, Hkv, group;
+  int causal;
+  float scale_log2;      // softmax scale * log2(e)
+  int n_mtiles;          // ceil(Sq / 128)
+  int pair_heads;        // 1: item = heads (2u, 2u+1) at one row tile
+  int n_units;           // head units per batch entry
+  int n_mslots;          // row-tile slots per unit
+  int n_items;
+  int n_kv_tiles;        // ceil(Sk / 128)
+  unsigned long long timeout_ns;
+  int inject_skip_load;  // test hook: index of a K/V load to drop (-1: none)
+  int* status;           // device status word (first error wins)
+};
+
+template <int D>
+struct Smem {
+  static constexpr int kChunks = D / 64;                  // 128-byte swizzle columns
+  static constexpr int kChunkBytes = 128 * 128;           // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kChunks * kChunkBytes;  // one Q/K/V tile
+  static constexpr int kStages = (D == 128) ? 4 : 6;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
+  //           o_full[2] o_empty[2] teardown
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
+};
+
+struct WorkItem {
+  int b, hq0, hq1, kvh, r0, r1;  // rows r_t .. r_t+127 of head hq_t
+  int n_kv;                       // key tiles [0, n_kv) to visit
+};
+
+// Number of 128-key tiles query rows [r0, r0+128) need (0 if none visible).
+__device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int r0) {
+  if (r0 >= p.Sq) return 0;
+  if (!p.causal) return p.n_kv_tiles;
+  int r_last = min(r0 + kBM - 1, p.Sq - 1);
+  long long lim = static_cast<long long>(r_last) + (p.Sk - p.Sq) + 1;  // exclusive key bound
+  if (lim <= 0) return 0;
+  if (lim > p.Sk) lim = p.Sk;
+  return static_cast<int>((lim + kBN - 1) / kBN);
+}
+
+// Work items are numbered longest first: row-tile slot descending (causal
+// cost grows with the row index), then batch, then head unit, so the heads of
+// one GQA group run side by side and share K/V through L2.
+__device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int idx) {
+  WorkItem w;
+  int per_slot = p.B * p.n_units;
+  int slot = p.n_mslots - 1 - idx / per_slot;
+  int rem = idx % per_slot;
+  w.b = rem / p.n_units;
+  int unit = rem % p.n_units;
+  if (p.pair_heads) {
+    w.hq0 = 2 * unit;
+    w.hq1 = 2 * unit + 1;
+    w.r0 = slot * kBM;
+    w.r1 = slot * kBM;
+  } else {
+    w.hq0 = unit;
+    w.hq1 = unit;
+    w.r0 = 2 * slot * kBM;
+    w.r1 = (2 * slot + 1) * kBM;
+  }
+  w.kvh = w.hq0 / p.group;
+  w.n_kv = max(kv_tiles_for(p, w.r0), kv_tiles_for(p, w.r1));
+  return w;
+}
+
+// Serpentine static schedule over the longest-first order: CTA c takes item
+// r*G + c on even rounds and r*G + (G-1-c) on odd rounds.
+__device__ __forceinline__ int item_of_round(int round, int cta, int grid) {
+  return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
+}
+
+// Bounded wait on an mbarrier phase. Returns false when the CTA aborted or the
+// wait ran past the time limit (which records kStatusTimeout and aborts).
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         const FwdParams& p) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+        atomicCAS(p.status, kStatusOk, kStatusTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) return ptx::pack_bf16x2(lo, hi);
+  else return ptx::pack_f16x2(lo, hi);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+  using L = Smem<D>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+
+  const uint32_t sQ = base + L::kQOff;
+  const uint32_t sKV = base + L::kKVOff;
+  const uint32_t bars = base + L::kBarOff;
+  const uint32_t bar_q_full = bars;                       // [2]
+  const uint32_t bar_q_empty = bars + 2 * 8;              // [2]
+  const uint32_t bar_kv_full = bars + 4 * 8;              // [kStages]
+  const uint32_t bar_kv_empty = bar_kv_full + kStages * 8;
+  const uint32_t bar_s_full = bar_kv_empty + kStages * 8;  // [2]
+  const uint32_t bar_p_full = bar_s_full + 2 * 8;          // [2]
+  const uint32_t bar_o_full = bar_p_full + 2 * 8;          // [2]
+  const uint32_t bar_o_empty = bar_o_full + 2 * 8;         // [2]
+  const uint32_t bar_teardown = bar_o_empty + 2 * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(bar_q_full + 8 * t, 1);
+      ptx::mbar_init(bar_q_empty + 8 * t, 1);
+      ptx::mbar_init(bar_s_full + 8 * t, 1);
+      ptx::mbar_init(bar_p_full + 8 * t, 128);
+      ptx::mbar_init(bar_o_full + 8 * t, 1);
+      ptx::mbar_init(bar_o_empty + 8 * t, 128);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar_kv_full + 8 * s, 1);
+      ptx::mbar_init(bar_kv_empty + 8 * s, 1);
+    }
+    ptx::mbar_init(bar_teardown, 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    ptx::prefetch_tensormap(&tm_q);
+    ptx::prefetch_tensormap(&tm_k);
+    ptx::prefetch_tensormap(&tm_v);
+  }
+  if (warp == kWarpMma) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int grid = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    const uint64_t pol_q = ptx::policy_evict_first();
+    uint32_t kv_it = 0, act = 0;
+    int load_idx = 0;
+    bool ok = true;
+    auto load_kv = [&](const CUtensorMap* map, int j, int kvh, int b) -> bool {
+      const uint32_t st = kv_it % kStages;
+      const uint32_t ph = ((kv_it / kStages) & 1u) ^ 1u;
+      if (!bar_wait(bar_kv_empty + 8 * st, ph, abort_flag, p)) return false;
+      if (lane == 0 && load_idx != p.inject_skip_load) {
+        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * st, L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_4d(sKV + st * L::kTileBytes + c * L::kChunkBytes, map, bar_kv_full + 8 * st, c * 64, kvh,
+                           j * kBN, b, pol_kv);
+      }
+      __syncwarp();
+      ++kv_it;
+      ++load_idx;
+      return true;
+    };
+    auto load_q = [&](int t, int hq, int r0, int b) -> bool {
+      if (!bar_wait(bar_q_empty + 8 * t, (act & 1u) ^ 1u, abort_flag, p)) return false;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar_q_full + 8 * t, L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_4d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tm_q, bar_q_full + 8 * t, c * 64, hq, r0,
+                           b, pol_q);
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int round = 0; ok; ++round) {
+      const int idx = item_of_round(round, cta, grid);
+      if (round * grid >= p.n_items) break;
+      if (idx >= p.n_items) continue;
+      const WorkItem w = decode_item(p, idx);
+      if (w.n_kv == 0) continue;
+      ok = load_q(0, w.hq0, w.r0, w.b) && load_kv(&tm_k, 0, w.kvh, w.b) && load_q(1, w.hq1, w.r1, w.b) &&
+           load_kv(&tm_v, 0, w.kvh, w.b);
+      for (int j = 1; ok && j < w.n_kv; ++j)
+        ok = load_kv(&tm_k, j, w.kvh, w.b) && load_kv(&tm_v, j, w.kvh, w.b);
+      ++act;
+    }
+    if (!ok && lane == 0) {
+      // Let copies already in flight land before the CTA leaves: wait (bounded)
+      // for the latest phase of every stage that was filled.
+      const uint64_t t0 = ptx::globaltimer_ns();
+      for (uint32_t k = (kv_it > (uint32_t)kStages ? kv_it - kStages : 0); k < kv_it; ++k) {
+        const uint32_t st = k % kStages, ph = (k / kStages) & 1u;
+        while (!ptx::mbar_try_wait(bar_kv_full + 8 * st, ph) && ptx::globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = ptx::idesc_f16(BF16, kBM, kBN, false, false);
+    constexpr uint32_t idesc_o = ptx::idesc_f16(BF16, kBM, D, false, true);
+    uint32_t kv_it = 0, act = 0;
+    uint32_t p_phase[2] = {0u, 0u};
+    bool ok = true;
+    // S_t = Q_t K^T over D: D/16 MMAs, K-major A and B, 128-byte swizzle.
+    auto issue_s = [&](int t, uint32_t k_stage) {
+      const uint32_t a0 = sQ + t * L::kTileBytes;
+      const uint32_t b0 = sKV + k_stage * L::kTileBytes;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks / 4) * L::kChunkBytes + (ks % 4) * 32;
+        ptx::mma_ss(tmem + (t ? kColS1 : kColS0), ptx::sdesc_sw128(a0 + off, 16, 1024),
+                    ptx::sdesc_sw128(b0 + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
+      }
+    };
+    // O_t (+)= P_t V over 128 keys: 8 MMAs, A = P from TMEM, B = V MN-major.
+    auto issue_pv = [&](int t, uint32_t v_stage, bool first) {
+      const uint32_t b0 = sKV + v_stage * L::kTileBytes;
+#pragma unroll
+      for (int ks = 0; ks < kBN / 16; ++ks) {
+        ptx::mma_ts(tmem + (t ? kColO1 : kColO0), tmem + (t ? kColS1 : kColS0) + ks * 8,
+                    ptx::sdesc_sw128(b0 + ks * 16 * 128, L::kChunkBytes, 1024), idesc_o,
+                    (first && ks == 0) ? 0u : 1u);
+      }
+    };
+    auto wait_stage = [&](uint32_t it) -> bool {
+      return bar_wait(bar_kv_full + 8 * (it % kStages), (it / kStages) & 1u, abort_flag, p);
+    };
+    for (int round = 0; ok; ++round) {
+      const int idx = item_of_round(round, cta, grid);
+      if (round * grid >= p.n_items) break;
+      if (idx >= p.n_items) continue;
+      const WorkItem w = decode_item(p, idx);
+      if (w.n_kv == 0) continue;
+      const uint32_t par = act & 1u;
+      ok = bar_wait(bar_q_full, par, abort_flag, p) && bar_wait(bar_q_full + 8, par, abort_flag, p) &&
+           wait_stage(kv_it);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t k_stage = kv_it % kStages;
+      if (lane == 0) {
+        issue_s(0, k_stage);
+        ptx::mma_commit(bar_s_full);
+        issue_s(1, k_stage);
+        ptx::mma_commit(bar_s_full + 8);
+        ptx::mma_commit(bar_kv_empty + 8 * k_stage);
+      }
+      __syncwarp();
+      ++kv_it;
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        const uint32_t v_stage = kv_it % kStages;
+        if (!(ok = wait_stage(kv_it))) break;
+        ++kv_it;
+        const bool more = (j + 1 < w.n_kv);
+        for (int t = 0; t < 2; ++t) {
+          if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
+          if (!(ok = bar_wait(bar_p_full + 8 * t, p_phase[t], abort_flag, p))) break;
+          p_phase[t] ^= 1u;
+          if (t == 0 && more) {
+            if (!(ok = wait_stage(kv_it))) break;
+            k_stage = kv_it % kStages;
+            ++kv_it;
+          }
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            issue_pv(t, v_stage, j == 0);
+            if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
+            if (more) {
+              issue_s(t, k_stage);
+              ptx::mma_commit(bar_s_full + 8 * t);
+              if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * k_stage);
+            } else {
+              ptx::mma_commit(bar_o_full + 8 * t);
+              ptx::mma_commit(bar_q_empty + 8 * t);
+            }
+          }
+          __syncwarp();
+        }
+      }
+      ++act;
+    }
+    if (!ok) {
+      // Wait (bounded) for every MMA already issued before TMEM is released.
+      if (lane == 0) ptx::mma_commit(bar_teardown);
+      __syncwarp();
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar_teardown, 0) && ptx::globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int row = threadIdx.x & 127;       // TMEM lane == row of the tile
+    const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + (t ? kColS1 : kColS0);
+    const uint32_t tO = tmem + lane_bits + (t ? kColO1 : kColO0);
+    const float sl2 = p.scale_log2;
+    const int offset = p.Sk - p.Sq;
+    uint32_t s_phase = 0, act = 0;
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+      const int idx = item_of_round(round, cta, grid);
+      if (round * grid >= p.n_items) break;
+      if (idx >= p.n_items) continue;
+      const WorkItem w = decode_item(p, idx);
+      const int hq = t ? w.hq1 : w.hq0;
+      const int r0 = t ? w.r1 : w.r0;
+      const int i = r0 + row;                // query row index
+      const bool row_valid = i < p.Sq;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      ((static_cast<long long>(w.b) * p.Sq + i) * p.Hq + hq) * (long long)D * 2;
+      if (w.n_kv == 0) {
+        if (row_valid) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < D * 2 / 16; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+          if (p.lse) p.lse[(static_cast<long long>(w.b) * p.Hq + hq) * p.Sq + i] = -__int_as_float(0x7f800000);
+        }
+        continue;
+      }
+      // exclusive key bound of this row (no key visible when <= 0)
+      int lim_abs = p.Sk;
+      if (p.causal) {
+        long long l2 = static_cast<long long>(i) + offset + 1;
+        lim_abs = static_cast<int>(l2 < 0 ? 0 : (l2 > p.Sk ? p.Sk : l2));
+      }
+      // key tiles from this one on need the mask for some row of this tile
+      int first_masked = p.n_kv_tiles;
+      if (p.Sk % kBN) first_masked = p.n_kv_tiles - 1;
+      if (p.causal) {
+        long long fm = (static_cast<long long>(r0) + offset + 1) / kBN;  // first tile not fully visible to row r0
+        if (static_cast<long long>(r0) + offset + 1 < 0) fm = 0;
+        if (fm < first_masked) first_masked = static_cast<int>(fm);
+      }
+      float m_ref = -__int_as_float(0x7f800000);
+      float l_exact = 0.0f, l_round = 0.0f;
+      for (int j = 0; j < w.n_kv; ++j) {
+        if (!(ok = bar_wait(bar_s_full + 8 * t, s_phase, abort_flag, p))) break;
+        s_phase ^= 1u;
+        ptx::tc_fence_after();
+        uint32_t sr[128];
+        ptx::tmem_ld_32x32b_x128(tS, sr);
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        if (j >= first_masked) {
+          const int lim = lim_abs - j * kBN;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -__int_as_float(0x7f800000);
+        }
+        // row max: four independent chains of three-input max
+        float mq0 = s[0], mq1 = s[1], mq2 = s[2], mq3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 8) {
+          mq0 = ptx::max3(mq0, s[c + 0], s[c + 1]);
+          mq1 = ptx::max3(mq1, s[c + 2], s[c + 3]);
+          mq2 = ptx::max3(mq2, s[c + 4], s[c + 5]);
+          mq3 = ptx::max3(mq3, s[c + 6], s[c + 7]);
+        }
+        const float mx = fmaxf(ptx::max3(mq0, mq1, mq2), mq3);
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        float alpha = 1.0f;
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        if (need) {
+          alpha = ptx::ex2_approx(m_ref - m_new);   // 0 when m_ref = -inf
+          m_ref = m_new;
+          l_exact *= alpha;
+          l_round *= alpha;
+        }
+        const float neg_m = (m_ref == -__int_as_float(0x7f800000)) ? 0.0f : -m_ref;
+        const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+        const uint64_t negm2 = ptx::f2_pack(neg_m, neg_m);
+        // p = 2^(s * scale * log2e - m); P is rounded to the input dtype for
+        // the P V product. l_exact sums the fp32 p (for LSE); l_round sums the
+        // rounded values the MMA multiplies, so O's weights sum to one.
+        uint32_t pk[64];
+        uint64_t acc_e0 = 0, acc_e1 = 0, acc_r0 = 0, acc_r1 = 0;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float t0, t1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2), t0, t1);
+          const float p0 = ptx::ex2_approx(t0), p1 = ptx::ex2_approx(t1);
+          pk[c] = pack2<BF16>(p0, p1);
+          float r0, r1;
+          if constexpr (BF16) {
+            r0 = __uint_as_float(pk[c] << 16);
+            r1 = __uint_as_float(pk[c] & 0xffff0000u);
+          } else {
+            ptx::f16x2_to_f32(pk[c], r0, r1);
+          }
+          if (c & 1) {
+            acc_e1 = ptx::f2_add(acc_e1, ptx::f2_pack(p0, p1));
+            acc_r1 = ptx::f2_add(acc_r1, ptx::f2_pack(r0, r1));
+          } else {
+            acc_e0 = ptx::f2_add(acc_e0, ptx::f2_pack(p0, p1));
+            acc_r0 = ptx::f2_add(acc_r0, ptx::f2_pack(r0, r1));
+          }
+        }
+        {
+          float a, b, c2, d;
+          ptx::f2_unpack(ptx::f2_add(acc_e0, acc_e1), a, b);
+          ptx::f2_unpack(ptx::f2_add(acc_r0, acc_r1), c2, d);
+          l_exact += a + b;
+          l_round += c2 + d;
+        }
+        ptx::tmem_st_32x32b_x64(tS, pk);
+        // Rescale O~ when some row of this warp raised its reference max. The
+        // previous P V of this tile completed before S of this key tile did.
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            ptx::tmem_ld_32x32b_x32(tO + c * 32, orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+            ptx::tmem_st_32x32b_x32(tO + c * 32, orr);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_p_full + 8 * t);
+      }
+      if (!ok) break;
+      // ---- epilogue: O = O~ / l, LSE = (m + log2 l) * ln 2
+      if (!(ok = bar_wait(bar_o_full + 8 * t, act & 1u, abort_flag, p))) break;
+      ptx::tc_fence_after();
+      uint32_t orr[D];
+      if constexpr (D == 128) {
+        ptx::tmem_ld_32x32b_x128(tO, orr);
+      } else {
+        ptx::tmem_ld_32x32b_x64(tO, orr);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_o_empty + 8 * t);
+      const bool live = l_exact > 0.0f;
+      const float inv_l = live ? __frcp_rn(l_round) : 0.0f;
+      if (row_valid) {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 v;
+          v.x = pack2<BF16>(__uint_as_float(orr[8 * c + 0]) * inv_l, __uint_as_float(orr[8 * c + 1]) * inv_l);
+          v.y = pack2<BF16>(__uint_as_float(orr[8 * c + 2]) * inv_l, __uint_as_float(orr[8 * c + 3]) * inv_l);
+          v.z = pack2<BF16>(__uint_as_float(orr[8 * c + 4]) * inv_l, __uint_as_float(orr[8 * c + 5]) * inv_l);
+          v.w = pack2<BF16>(__uint_as_float(orr[8 * c + 6]) * inv_l, __uint_as_float(orr[8 * c + 7]) * inv_l);
+          reinterpret_cast<uint4*>(orow)[c] = v;
+        }
+        if (p.lse) {
+          const float lse = live ? (m_ref + __log2f(l_exact)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
+          p.lse[(static_cast<long long>(w.b) * p.Hq + hq) * p.Sq + i] = lse;
+        }
+      }
+      ++act;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace fa

@@ -1,0 +1,107 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) FlashAttention forward library.
+ *
+ * The library computes exact softmax attention
+ *
+ *     O = softmax(scale * Q K^T + M) V,     LSE = logsumexp(scale * Q K^T + M)
+ *
+ * row by row, tile by tile with online softmax, so the Sq x Sk score and
+ * probability matrices never reach device memory. Sources:
+ *   - "MiniPaged-Qwen: Qwen3 Prefill FlashAttention" (blog.zsmgc.love),
+ *     section 1 (the operation and the causal mask M), sections 3.1 and 4
+ *     (tiling and the online-softmax recurrence), section 6 (GQA head map
+ *     kv_head = q_head / (Hq / Hkv)), section 13 (bottom-right causal limit
+ *     causal_limit = kv_len - q_len + qi + 1);
+ *   - "NVIDIA闪存注意力实操：极速提升4倍性能" (nmedialink.com), sections
+ *     "在线Softmax算法" and "因果注意力与分组查询注意力";
+ *   - "FlashAttention 个人实现思路" (blueriverlhr.github.io), introduction
+ *     (the (batch, seq_len, n_heads, d_head) layout) and the kernel argument
+ *     struct (contiguous strided tensors).
+ * LSE is not defined on any page; here it is the natural-log log-sum-exp of
+ * the scaled, masked scores of each query row.
+ *
+ * Every function is thread-safe and returns an fa_status_t code. Nothing
+ * here allocates or frees caller memory.
+ */
+#ifndef FA_GB300_H_
+#define FA_GB300_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle; the same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* a pointer, size, alignment or flag is invalid */
+  FA_ERR_UNSUPPORTED = 2,  /* valid request outside what the kernel covers */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 4       /* a device-side bounded wait ran out (see fa_status) */
+} fa_status_t;
+
+typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype_t;
+
+/*
+ * fa_fwd — attention forward on one GPU, enqueued on `stream`.
+ *
+ * q    device pointer, (B, Sq, Hq, D) contiguous, element type `dtype`
+ * k, v device pointers, (B, Sk, Hkv, D) contiguous, element type `dtype`
+ * o    device pointer, (B, Sq, Hq, D) contiguous, written (fully overwritten)
+ * lse  device pointer, (B, Hq, Sq) contiguous float32 (natural log), or NULL
+ *      to skip it. Rows that see no key get O = 0 and LSE = -inf.
+ * B, Sq, Sk, Hq, Hkv, D   sizes; Hq must be a multiple of Hkv (query head h
+ *      reads key/value head h / (Hq / Hkv)); D must be 64 or 128.
+ * scale  softmax scale (1/sqrt(D) in the usual case); finite and > 0.
+ * causal 0: every key is visible; 1: bottom-right causal mask, query i sees
+ *      key j iff j <= i + Sk - Sq (top-left when Sq == Sk).
+ * dtype  FA_DTYPE_FP16 or FA_DTYPE_BF16 (inputs and O share it; P is rounded
+ *      to it before the P V product; accumulation is fp32).
+ * stream CUDA stream of the current device (NULL = legacy default stream).
+ *
+ * Ownership: the caller allocates and owns every buffer; q, k and v are only
+ * read. The library keeps a per-device status word and no other state.
+ * Alignment: q, k, v, o must be 16-byte aligned; lse 4-byte aligned.
+ * Errors: arguments are checked before anything is enqueued. Negative sizes,
+ * NULL pointers, Hkv == 0 or Hq % Hkv != 0, a non-finite or non-positive
+ * scale, causal not in {0,1}, dtype not in {0,1} or a misaligned pointer give
+ * FA_ERR_INVALID_ARG; D not in {64, 128} or sizes whose element offsets do not
+ * fit the kernel's 32-bit tile coordinates give FA_ERR_UNSUPPORTED. With
+ * B, Sq or Hq equal to 0 nothing is written and FA_OK is returned. Sk == 0 is
+ * valid: O = 0 and LSE = -inf. A failed launch returns FA_ERR_CUDA. The call
+ * is asynchronous; a device-side timeout is reported later by fa_status().
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk, int Hq,
+           int Hkv, int D, float scale, int causal, int dtype, fa_stream_t stream);
+
+/*
+ * fa_status — synchronise `stream`, then read and clear the device status
+ * word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's bounded
+ * wait on an mbarrier ran out (the kernel then released its tensor memory
+ * and returned; the CUDA context stays usable). FA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int fa_status(fa_stream_t stream);
+
+/* fa_status_string — static, human-readable name of a status code. */
+const char* fa_status_string(int code);
+
+/* fa_version — library version as major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+/*
+ * fa_debug_set_fault — test hook for failure detection. With `skip_load`
+ * >= 0 every later fa_fwd launch on this process drops its K/V load number
+ * `skip_load` (counted per CTA), so the consumer's bounded wait runs out after
+ * `timeout_ms` milliseconds (<= 0 keeps the default of 2000 ms) and the kernel
+ * records FA_ERR_TIMEOUT. -1 restores normal operation. The default timeout
+ * is also overridable with the environment variable FA_WAIT_TIMEOUT_MS.
+ */
+int fa_debug_set_fault(int skip_load, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H_ */

@@ -1,0 +1,91 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every
+entry point include/fa.h declares, and rejects invalid arguments before it
+touches the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_16_gb300 import api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(api.library_path()):
+        from exact_attention_16_gb300 import build
+        build.build()
+    return api.lib()
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    assert {"fa_fwd", "fa_status", "fa_status_string", "fa_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert name in api.EXPORTED_SYMBOLS, name
+
+
+def test_version_and_status_strings(lib):
+    assert api.fa_version() >= 100
+    assert api.fa_status_string(0) == "FA_OK"
+    assert api.fa_status_string(4) == "FA_ERR_TIMEOUT"
+    assert api.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def _call(lib, **kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=None, B=1, Sq=4, Sk=4, Hq=2, Hkv=1, D=128,
+                scale=0.125, causal=0, dtype=1, stream=None)
+    args.update(kw)
+    return lib.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["Sq"],
+                      args["Sk"], args["Hq"], args["Hkv"], args["D"], ctypes.c_float(args["scale"]),
+                      args["causal"], args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), api.FA_ERR_INVALID_ARG),
+    (dict(Sq=-3), api.FA_ERR_INVALID_ARG),
+    (dict(Sk=-1), api.FA_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), api.FA_ERR_INVALID_ARG),
+    (dict(Hkv=0), api.FA_ERR_INVALID_ARG),
+    (dict(dtype=2), api.FA_ERR_INVALID_ARG),
+    (dict(causal=2), api.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), api.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), api.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), api.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), api.FA_ERR_INVALID_ARG),
+    (dict(q=None), api.FA_ERR_INVALID_ARG),
+    (dict(o=None), api.FA_ERR_INVALID_ARG),
+    (dict(k=None), api.FA_ERR_INVALID_ARG),
+    (dict(q=24), api.FA_ERR_INVALID_ARG),       # not 16-byte aligned
+    (dict(v=8), api.FA_ERR_INVALID_ARG),
+    (dict(lse=2), api.FA_ERR_INVALID_ARG),      # not 4-byte aligned
+    (dict(D=96), api.FA_ERR_UNSUPPORTED),
+    (dict(D=256), api.FA_ERR_UNSUPPORTED),
+    (dict(B=0), api.FA_OK),                     # nothing to do: no device call
+    (dict(Sq=0), api.FA_OK),
+    (dict(Hq=0, Hkv=1), api.FA_OK),
+])
+def test_invalid_arguments_are_rejected_before_any_launch(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_sk_zero_needs_no_kv_pointers_but_still_validates(lib):
+    assert _call(lib, Sk=0, k=None, v=None, D=96) == api.FA_ERR_UNSUPPORTED
+
+
+def test_debug_fault_hook_validates(lib):
+    assert api.fa_debug_set_fault(-2) == api.FA_ERR_INVALID_ARG
+    assert api.fa_debug_set_fault(-1) == api.FA_OK

@@ -1,0 +1,104 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+Small and ragged shapes are compared on every element; the five full-size
+workloads run in the exact launch configuration the bench times and are
+compared on sampled rows (first/last tiles, a middle tile boundary, random
+rows) of several (batch, head) pairs.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from exact_attention_16_gb300 import api  # noqa: E402
+from exact_attention_16_gb300.workloads import WORKLOADS, Workload  # noqa: E402
+
+from parity import check_full, check_sampled, run_gpu  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def W(B, Sq, Sk, Hq, Hkv, D, dtype="bf16", causal=False, sigma=1.0, seed=7):
+    return Workload("case", B, Sq, Sk, Hq, Hkv, D, dtype, causal, sigma, 1.0, seed)
+
+
+# ---- one tile, then several tiles and ragged tails, both head pairings
+SMALL = [
+    W(1, 128, 128, 2, 2, 128),                       # one tile pair, MHA (row-tile pairs)
+    W(1, 128, 128, 2, 1, 128),                       # GQA 2:1 (head pairs)
+    W(1, 128, 128, 2, 2, 64),
+    W(1, 256, 256, 4, 2, 128, causal=True),
+    W(1, 300, 257, 4, 4, 128, causal=False),         # ragged query and key tails
+    W(1, 300, 257, 4, 4, 128, causal=True),          # Sq > Sk: first rows see nothing
+    W(2, 257, 300, 8, 2, 128, "fp16", causal=True),  # Sk > Sq: offset 43
+    W(1, 1, 1, 2, 1, 128),
+    W(1, 1, 77, 2, 2, 64, causal=True),              # one query sees every key
+    W(1, 77, 1, 2, 2, 64, causal=True),              # only the last row sees the key
+    W(1, 520, 520, 6, 2, 64, "fp16", causal=True),   # G = 3 (odd): row-tile pairs
+    W(2, 384, 640, 8, 8, 128, causal=True, sigma=2.0),   # sharp softmax: |O| up to ~4.5
+    W(1, 2048, 2048, 4, 2, 128, causal=True, sigma=2.0),
+    W(1, 1000, 1000, 4, 1, 128, "fp16", causal=True, sigma=2.0),
+    W(1, 640, 384, 4, 1, 128, causal=True),          # G = 4
+    W(1, 129, 1000, 32, 4, 128, causal=False),       # G = 8
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: f"B{w.B}_Sq{w.Sq}_Sk{w.Sk}_H{w.Hq}-{w.Hkv}_D{w.D}_{w.dtype}_{'c' if w.causal else 'n'}")
+def test_small_shapes_every_element(w):
+    check_full(w)
+
+
+def test_workload_tiny_every_element():
+    check_full(WORKLOADS[0])
+
+
+def test_workload_causal_mha_offset_every_element():
+    check_full(WORKLOADS[1])
+
+
+@pytest.mark.parametrize("w", WORKLOADS[2:], ids=lambda w: w.name)
+def test_full_size_workloads_sampled_rows(w):
+    check_sampled(w)
+
+
+@pytest.mark.parametrize("w", WORKLOADS[2:], ids=lambda w: w.name)
+def test_full_size_workloads_every_row_of_two_heads(w):
+    check_sampled(w, heads={(0, 1), (w.B - 1, w.Hq - 2)}, all_rows=True)
+
+
+def test_sk_zero_gives_zero_output_and_neg_inf_lse():
+    q = torch.randn(1, 5, 2, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty(1, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    o, lse = api.fa_fwd(q, k, k.clone(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(lse == float("-inf"))
+
+
+def test_lse_optional_and_output_overwritten():
+    w = W(1, 200, 200, 2, 2, 128, causal=True)
+    from exact_attention_16_gb300.workloads import draw_inputs
+    q, k, v = (t.cuda() for t in draw_inputs(w))
+    o_ref, _ = api.fa_fwd(q, k, v, causal=True)
+    out = torch.full_like(q, float("nan"))
+    o2, l2 = api.fa_fwd(q, k, v, causal=True, out=out, return_lse=False)
+    torch.cuda.synchronize()
+    assert l2 is None and torch.equal(o2, o_ref)
+
+
+def test_repeatable_and_stream_ordered():
+    w = W(1, 512, 512, 4, 2, 128, causal=True)
+    from exact_attention_16_gb300.workloads import draw_inputs
+    q, k, v = (t.cuda() for t in draw_inputs(w))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1 = api.fa_fwd(q, k, v, causal=True)
+        o2, l2 = api.fa_fwd(q, k, v, causal=True)
+    s.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
