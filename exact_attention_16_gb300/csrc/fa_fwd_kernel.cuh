@@ -65,9 +65,9 @@ struct Smem {
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
-  //           o_full[2] o_empty[2] teardown
-  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1;
+  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_lo[2]
+  //           p_hi[2] o_full[2] o_empty[2] teardown
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
@@ -168,8 +168,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const uint32_t bar_kv_full = bars + 4 * 8;              // [kStages]
   const uint32_t bar_kv_empty = bar_kv_full + kStages * 8;
   const uint32_t bar_s_full = bar_kv_empty + kStages * 8;  // [2]
-  const uint32_t bar_p_full = bar_s_full + 2 * 8;          // [2]
-  const uint32_t bar_o_full = bar_p_full + 2 * 8;          // [2]
+  const uint32_t bar_p_lo = bar_s_full + 2 * 8;            // [2] P columns 0..31 (keys 0..63) written
+  const uint32_t bar_p_hi = bar_p_lo + 2 * 8;              // [2] P columns 32..63 (keys 64..127) written
+  const uint32_t bar_o_full = bar_p_hi + 2 * 8;            // [2]
   const uint32_t bar_o_empty = bar_o_full + 2 * 8;         // [2]
   const uint32_t bar_teardown = bar_o_empty + 2 * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::kMiscOff);
@@ -183,7 +184,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_init(bar_q_full + 8 * t, 1);
       ptx::mbar_init(bar_q_empty + 8 * t, 1);
       ptx::mbar_init(bar_s_full + 8 * t, 1);
-      ptx::mbar_init(bar_p_full + 8 * t, 128);
+      ptx::mbar_init(bar_p_lo + 8 * t, 128);
+      ptx::mbar_init(bar_p_hi + 8 * t, 128);
       ptx::mbar_init(bar_o_full + 8 * t, 1);
       ptx::mbar_init(bar_o_empty + 8 * t, 128);
     }
@@ -271,29 +273,40 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
+    // Pipe order per key tile j: P0 V_j (two halves), Q0 K_{j+1}^T, P1 V_j,
+    // Q1 K_{j+1}^T. The P V halves start as soon as the softmax has written
+    // the matching half of P.
     constexpr uint32_t idesc_s = ptx::idesc_f16(BF16, kBM, kBN, false, false);
     constexpr uint32_t idesc_o = ptx::idesc_f16(BF16, kBM, D, false, true);
-    uint32_t kv_it = 0, act = 0;
-    uint32_t p_phase[2] = {0u, 0u};
+    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // descriptor units per ring stage
+    // Descriptor bases; the start-address field (bits 0..13) is advanced by
+    // adding byte offsets >> 4 (shared addresses stay below 256 KB).
+    const uint64_t dq0 = ptx::sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dq1 = ptx::sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
+    const uint64_t dk0 = ptx::sdesc_sw128(sKV, 16, 1024);                 // K: K-major
+    const uint64_t dv0 = ptx::sdesc_sw128(sKV, L::kChunkBytes, 1024);     // V: MN-major
+    uint32_t kv_it = 0, act = 0, p_phase[2] = {0u, 0u};
     bool ok = true;
-    // S_t = Q_t K^T over D: D/16 MMAs, K-major A and B, 128-byte swizzle.
-    auto issue_s = [&](int t, uint32_t k_stage) {
-      const uint32_t a0 = sQ + t * L::kTileBytes;
-      const uint32_t b0 = sKV + k_stage * L::kTileBytes;
+    // S_t = Q_t K^T: D/16 MMAs over the head dimension.
+    auto issue_s = [&](int t, uint32_t st) {
+      const uint64_t a = t ? dq1 : dq0;
+      const uint64_t bk = dk0 + st * kStageDesc;
+      const uint32_t d = tmem + (t ? kColS1 : kColS0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = (ks / 4) * L::kChunkBytes + (ks % 4) * 32;
-        ptx::mma_ss(tmem + (t ? kColS1 : kColS0), ptx::sdesc_sw128(a0 + off, 16, 1024),
-                    ptx::sdesc_sw128(b0 + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
+        const uint32_t off = static_cast<uint32_t>(((ks / 4) * L::kChunkBytes + (ks % 4) * 32) >> 4);
+        ptx::mma_ss(d, a + off, bk + off, idesc_s, ks > 0 ? 1u : 0u);
       }
     };
-    // O_t (+)= P_t V over 128 keys: 8 MMAs, A = P from TMEM, B = V MN-major.
-    auto issue_pv = [&](int t, uint32_t v_stage, bool first) {
-      const uint32_t b0 = sKV + v_stage * L::kTileBytes;
+    // O_t (+)= P_t V for keys [64 h, 64 h + 64): 4 MMAs, P from TMEM.
+    auto issue_pv = [&](int t, uint32_t st, int h, bool first) {
+      const uint64_t bv = dv0 + st * kStageDesc;
+      const uint32_t d = tmem + (t ? kColO1 : kColO0);
+      const uint32_t pa = tmem + (t ? kColS1 : kColS0);
 #pragma unroll
-      for (int ks = 0; ks < kBN / 16; ++ks) {
-        ptx::mma_ts(tmem + (t ? kColO1 : kColO0), tmem + (t ? kColS1 : kColS0) + ks * 8,
-                    ptx::sdesc_sw128(b0 + ks * 16 * 128, L::kChunkBytes, 1024), idesc_o,
+      for (int k = 0; k < 4; ++k) {
+        const int ks = 4 * h + k;
+        ptx::mma_ts(d, pa + ks * 8, bv + static_cast<uint32_t>((ks * 16 * 128) >> 4), idesc_o,
                     (first && ks == 0) ? 0u : 1u);
       }
     };
@@ -307,17 +320,23 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const WorkItem w = decode_item(p, idx);
       if (w.n_kv == 0) continue;
       const uint32_t par = act & 1u;
-      ok = bar_wait(bar_q_full, par, abort_flag, p) && bar_wait(bar_q_full + 8, par, abort_flag, p) &&
-           wait_stage(kv_it);
-      if (!ok) break;
-      ptx::tc_fence_after();
       uint32_t k_stage = kv_it % kStages;
+      // prologue: S_0 = Q_0 K_0^T as soon as Q_0 and K_0 land, then S_1
+      if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_stage(kv_it))) break;
+      ptx::tc_fence_after();
       if (lane == 0) {
         issue_s(0, k_stage);
         ptx::mma_commit(bar_s_full);
+        if (w.n_kv == 1) ptx::mma_commit(bar_q_empty);
+      }
+      __syncwarp();
+      if (!(ok = bar_wait(bar_q_full + 8, par, abort_flag, p))) break;
+      ptx::tc_fence_after();
+      if (lane == 0) {
         issue_s(1, k_stage);
         ptx::mma_commit(bar_s_full + 8);
         ptx::mma_commit(bar_kv_empty + 8 * k_stage);
+        if (w.n_kv == 1) ptx::mma_commit(bar_q_empty + 8);
       }
       __syncwarp();
       ++kv_it;
@@ -326,29 +345,37 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!(ok = wait_stage(kv_it))) break;
         ++kv_it;
         const bool more = (j + 1 < w.n_kv);
+        const bool last_s = (j + 2 == w.n_kv);   // S_t(j+1) is the item's last use of Q_t
         for (int t = 0; t < 2; ++t) {
           if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-          if (!(ok = bar_wait(bar_p_full + 8 * t, p_phase[t], abort_flag, p))) break;
+          if (!(ok = bar_wait(bar_p_lo + 8 * t, p_phase[t], abort_flag, p))) break;
+          ptx::tc_fence_after();
+          if (lane == 0) issue_pv(t, v_stage, 0, j == 0);
+          __syncwarp();
+          if (!(ok = bar_wait(bar_p_hi + 8 * t, p_phase[t], abort_flag, p))) break;
           p_phase[t] ^= 1u;
-          if (t == 0 && more) {
-            if (!(ok = wait_stage(kv_it))) break;
-            k_stage = kv_it % kStages;
-            ++kv_it;
-          }
           ptx::tc_fence_after();
           if (lane == 0) {
-            issue_pv(t, v_stage, j == 0);
+            issue_pv(t, v_stage, 1, j == 0);
             if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
-            if (more) {
+            if (!more) ptx::mma_commit(bar_o_full + 8 * t);
+          }
+          __syncwarp();
+          if (more) {
+            if (t == 0) {
+              if (!(ok = wait_stage(kv_it))) break;
+              k_stage = kv_it % kStages;
+              ++kv_it;
+              ptx::tc_fence_after();
+            }
+            if (lane == 0) {
               issue_s(t, k_stage);
               ptx::mma_commit(bar_s_full + 8 * t);
               if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * k_stage);
-            } else {
-              ptx::mma_commit(bar_o_full + 8 * t);
-              ptx::mma_commit(bar_q_empty + 8 * t);
+              if (last_s) ptx::mma_commit(bar_q_empty + 8 * t);
             }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       ++act;
@@ -407,7 +434,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (fm < first_masked) first_masked = static_cast<int>(fm);
       }
       float m_ref = -__int_as_float(0x7f800000);
-      float l_exact = 0.0f, l_round = 0.0f;
+      float l_exact = 0.0f, l_corr = 0.0f;
       for (int j = 0; j < w.n_kv; ++j) {
         if (!(ok = bar_wait(bar_s_full + 8 * t, s_phase, abort_flag, p))) break;
         s_phase ^= 1u;
@@ -422,16 +449,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -__int_as_float(0x7f800000);
         }
-        // row max: four independent chains of three-input max
-        float mq0 = s[0], mq1 = s[1], mq2 = s[2], mq3 = s[3];
+        // row max: eight independent chains of three-input max
+        float mq[8];
 #pragma unroll
-        for (int c = 4; c < 128; c += 8) {
-          mq0 = ptx::max3(mq0, s[c + 0], s[c + 1]);
-          mq1 = ptx::max3(mq1, s[c + 2], s[c + 3]);
-          mq2 = ptx::max3(mq2, s[c + 4], s[c + 5]);
-          mq3 = ptx::max3(mq3, s[c + 6], s[c + 7]);
+        for (int c = 0; c < 8; ++c) mq[c] = s[c];
+#pragma unroll
+        for (int c = 8; c < 128; c += 16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mq[q] = ptx::max3(mq[q], s[c + 2 * q], s[c + 2 * q + 1]);
         }
-        const float mx = fmaxf(ptx::max3(mq0, mq1, mq2), mq3);
+        const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
         const float m_new = fmaxf(m_ref, mx * sl2);
         float alpha = 1.0f;
         const bool need = m_new > m_ref + kRescaleThreshold;
@@ -439,60 +466,82 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           alpha = ptx::ex2_approx(m_ref - m_new);   // 0 when m_ref = -inf
           m_ref = m_new;
           l_exact *= alpha;
-          l_round *= alpha;
+          l_corr *= alpha;
         }
         const float neg_m = (m_ref == -__int_as_float(0x7f800000)) ? 0.0f : -m_ref;
         const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
         const uint64_t negm2 = ptx::f2_pack(neg_m, neg_m);
-        // p = 2^(s * scale * log2e - m); P is rounded to the input dtype for
-        // the P V product. l_exact sums the fp32 p (for LSE); l_round sums the
-        // rounded values the MMA multiplies, so O's weights sum to one.
-        uint32_t pk[64];
-        uint64_t acc_e0 = 0, acc_e1 = 0, acc_r0 = 0, acc_r1 = 0;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float t0, t1;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2), t0, t1);
-          const float p0 = ptx::ex2_approx(t0), p1 = ptx::ex2_approx(t1);
-          pk[c] = pack2<BF16>(p0, p1);
-          float r0, r1;
-          if constexpr (BF16) {
-            r0 = __uint_as_float(pk[c] << 16);
-            r1 = __uint_as_float(pk[c] & 0xffff0000u);
-          } else {
-            ptx::f16x2_to_f32(pk[c], r0, r1);
-          }
-          if (c & 1) {
-            acc_e1 = ptx::f2_add(acc_e1, ptx::f2_pack(p0, p1));
-            acc_r1 = ptx::f2_add(acc_r1, ptx::f2_pack(r0, r1));
-          } else {
-            acc_e0 = ptx::f2_add(acc_e0, ptx::f2_pack(p0, p1));
-            acc_r0 = ptx::f2_add(acc_r0, ptx::f2_pack(r0, r1));
-          }
-        }
+        // p = 2^(s * scale * log2e - m). P is rounded to the input dtype for the
+        // P V product; l_exact sums the unrounded fp32 p (it gives LSE). The
+        // largest p of this tile (the element equal to the tile max) is also
+        // rounded here, and its rounding error is added to l_corr, so that O is
+        // normalised by the sum of the weights the MMA actually used for the
+        // dominant terms: when one key dominates a row, O reproduces its value.
+        uint64_t acc0 = 0, acc1 = 0;
         {
-          float a, b, c2, d;
-          ptx::f2_unpack(ptx::f2_add(acc_e0, acc_e1), a, b);
-          ptx::f2_unpack(ptx::f2_add(acc_r0, acc_r1), c2, d);
-          l_exact += a + b;
-          l_round += c2 + d;
+          const float pmax = ptx::ex2_approx(fmaf(mx, sl2, neg_m));
+          const uint32_t pr = pack2<BF16>(pmax, 0.0f);
+          float pmax_r;
+          if constexpr (BF16) {
+            pmax_r = __uint_as_float(pr << 16);
+          } else {
+            float hi_unused;
+            ptx::f16x2_to_f32(pr, pmax_r, hi_unused);
+          }
+          l_corr += pmax_r - pmax;
         }
-        ptx::tmem_st_32x32b_x64(tS, pk);
+        auto exp_half = [&](int h, uint32_t (&pk)[32]) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int e = 64 * h + 2 * c;
+            float t0, t1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[e], s[e + 1]), sl2x2, negm2), t0, t1);
+            const float p0 = ptx::ex2_approx(t0), p1 = ptx::ex2_approx(t1);
+            pk[c] = pack2<BF16>(p0, p1);
+            if (c & 1) acc1 = ptx::f2_add(acc1, ptx::f2_pack(p0, p1));
+            else acc0 = ptx::f2_add(acc0, ptx::f2_pack(p0, p1));
+          }
+        };
+        {
+          uint32_t pk[32];
+          exp_half(0, pk);
+          ptx::tmem_st_32x32b_x32(tS, pk);
+        }
         // Rescale O~ when some row of this warp raised its reference max. The
         // previous P V of this tile completed before S of this key tile did.
         if (j > 0 && __any_sync(0xffffffffu, need)) {
+          const uint64_t a2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t orr[32];
             ptx::tmem_ld_32x32b_x32(tO + c * 32, orr);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+            for (int e = 0; e < 32; e += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2),
+                             x0, x1);
+              orr[e] = __float_as_uint(x0);
+              orr[e + 1] = __float_as_uint(x1);
+            }
             ptx::tmem_st_32x32b_x32(tO + c * 32, orr);
           }
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_p_full + 8 * t);
+        ptx::mbar_arrive(bar_p_lo + 8 * t);
+        {
+          uint32_t pk[32];
+          exp_half(1, pk);
+          ptx::tmem_st_32x32b_x32(tS + 32, pk);
+        }
+        {
+          float a0, a1;
+          ptx::f2_unpack(ptx::f2_add(acc0, acc1), a0, a1);
+          l_exact += a0 + a1;
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_p_hi + 8 * t);
       }
       if (!ok) break;
       // ---- epilogue: O = O~ / l, LSE = (m + log2 l) * ln 2
@@ -507,7 +556,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_o_empty + 8 * t);
       const bool live = l_exact > 0.0f;
-      const float inv_l = live ? __frcp_rn(l_round) : 0.0f;
+      const float inv_l = live ? __frcp_rn(l_exact + l_corr) : 0.0f;
       if (row_valid) {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
