@@ -125,7 +125,7 @@ __device__ __forceinline__ int item_of_round(int round, int cta, int grid) {
 // wait ran past the time limit (which records kStatusTimeout and aborts).
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          const FwdParams& p) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (ptx::mbar_test_wait(bar, parity)) return true;
   uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -341,41 +341,51 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       __syncwarp();
       ++kv_it;
       for (int j = 0; ok && j < w.n_kv; ++j) {
-        const uint32_t v_stage = kv_it % kStages;
-        if (!(ok = wait_stage(kv_it))) break;
-        ++kv_it;
         const bool more = (j + 1 < w.n_kv);
         const bool last_s = (j + 2 == w.n_kv);   // S_t(j+1) is the item's last use of Q_t
+        const uint32_t v_stage = kv_it % kStages;
+        // V_j and (when there is one) K_{j+1} are normally resident long before
+        // they are needed; wait for both here so that each tile's P V and next
+        // Q K^T go out as one uninterrupted run of MMAs.
+        if (!(ok = wait_stage(kv_it))) break;
+        ++kv_it;
+        if (more) {
+          if (!(ok = wait_stage(kv_it))) break;
+          k_stage = kv_it % kStages;
+          ++kv_it;
+        }
         for (int t = 0; t < 2; ++t) {
           if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
           if (!(ok = bar_wait(bar_p_lo + 8 * t, p_phase[t], abort_flag, p))) break;
-          ptx::tc_fence_after();
-          if (lane == 0) issue_pv(t, v_stage, 0, j == 0);
-          __syncwarp();
-          if (!(ok = bar_wait(bar_p_hi + 8 * t, p_phase[t], abort_flag, p))) break;
-          p_phase[t] ^= 1u;
-          ptx::tc_fence_after();
-          if (lane == 0) {
-            issue_pv(t, v_stage, 1, j == 0);
-            if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
-            if (!more) ptx::mma_commit(bar_o_full + 8 * t);
-          }
-          __syncwarp();
-          if (more) {
-            if (t == 0) {
-              if (!(ok = wait_stage(kv_it))) break;
-              k_stage = kv_it % kStages;
-              ++kv_it;
-              ptx::tc_fence_after();
-            }
+          if (ptx::mbar_test_wait(bar_p_hi + 8 * t, p_phase[t])) {
+            // all of P_t(j) is written: one run of 8 P V MMAs
+            ptx::tc_fence_after();
             if (lane == 0) {
+              issue_pv(t, v_stage, 0, j == 0);
+              issue_pv(t, v_stage, 1, j == 0);
+            }
+          } else {
+            // the softmax is still on keys 64..127: start on keys 0..63
+            ptx::tc_fence_after();
+            if (lane == 0) issue_pv(t, v_stage, 0, j == 0);
+            __syncwarp();
+            if (!(ok = bar_wait(bar_p_hi + 8 * t, p_phase[t], abort_flag, p))) break;
+            ptx::tc_fence_after();
+            if (lane == 0) issue_pv(t, v_stage, 1, j == 0);
+          }
+          p_phase[t] ^= 1u;
+          if (lane == 0) {
+            if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
+            if (more) {
               issue_s(t, k_stage);
               ptx::mma_commit(bar_s_full + 8 * t);
               if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * k_stage);
               if (last_s) ptx::mma_commit(bar_q_empty + 8 * t);
+            } else {
+              ptx::mma_commit(bar_o_full + 8 * t);
             }
-            __syncwarp();
           }
+          __syncwarp();
         }
       }
       ++act;
