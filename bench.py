@@ -132,6 +132,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """Largest `value` over all ranks (the slowest rank's time); identity
+    when `dist` is None. A control-plane reduction, not part of the step."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flop_per_step: int, steps: int, max_ms: float) -> float:
+    """Aggregate throughput: every rank ran `steps` steps of `flop_per_step`
+    (weak scaling); the job took as long as the slowest rank."""
+    return world * flop_per_step * steps / (max_ms * 1e-3) / 1e12
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -195,10 +213,7 @@ def run_ours(args, w):
         raise RuntimeError("device status not OK after the timed region")
     launch_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
     total_ms = starts[0].elapsed_time(ends[-1]) if flush is None else sum(launch_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
 
     # end to end through the same public call with pinned host buffers:
     # H2D of q, k, v, the kernel, and D2H of O and LSE every step
@@ -223,18 +238,14 @@ def run_ours(args, w):
     for _ in range(e2e_steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     h2d = in_bytes
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
 
     peaks = measured_peaks()
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
     achieved = flop / (avg_launch_ms * 1e-3) / 1e12
-    value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flop, args.steps, total_ms)
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -268,7 +279,7 @@ def run_ours(args, w):
             "avg_launch_ms": round(avg_launch_ms, 4),
         },
         "e2e": {
-            "value": round(world * flop * e2e_steps / e2e_s / 1e12, 2),
+            "value": round(whole_job_tflops(world, flop, e2e_steps, e2e_s * 1e3), 2),
             "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
@@ -303,9 +314,13 @@ def cpu_baseline(w, q, k, v, budget_s: float):
     rows = min(w.Sq, 256)
     heads = 1
     secs, flop = oracle_sample(w, q32, k32, v32, rows, heads)
-    # grow the sample until it takes about `budget_s`
-    while secs < budget_s * 0.5 and heads < 4 * w.B * w.Hq:
-        heads *= 2
+    # grow the sample (more heads, then more rows per head) until one pass
+    # takes at least two thirds of `budget_s`
+    while secs < budget_s * 0.66 and (heads < w.B * w.Hq or rows < w.Sq):
+        if heads < w.B * w.Hq:
+            heads = min(w.B * w.Hq, heads * 2)
+        else:
+            rows = min(w.Sq, rows * 2)
         secs, flop = oracle_sample(w, q32, k32, v32, rows, heads)
     return {
         "value": round(flop / secs / 1e12, 6),
@@ -370,7 +385,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[x.name for x in WORKLOADS])
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=18.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
