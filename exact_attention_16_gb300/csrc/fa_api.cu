@@ -88,16 +88,16 @@ DeviceState* device_state(int* dev_out) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // 4-D map over a (B, S, H, D) tensor: dims innermost first (D, H, S, B); the
-// box is 64 elements (128 bytes) x 1 head x 128 rows x 1 batch, 128-byte
-// swizzle, zero fill outside the tensor.
-bool encode_bshd(CUtensorMap* map, const void* ptr, bool bf16, int B, int S, int H, int D) {
+// box is 64 elements (128 bytes) x 1 head x `box_rows` rows x 1 batch,
+// 128-byte swizzle, zero fill outside the tensor (loads) / clipping (stores).
+bool encode_bshd(CUtensorMap* map, const void* ptr, bool bf16, int B, int S, int H, int D, int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                               static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
                                  static_cast<cuuint64_t>(S) * H * D * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -117,10 +117,10 @@ unsigned long long wait_timeout_ns() {
 }
 
 template <int D, bool BF16>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::FwdParams& p, int grid,
-           cudaStream_t stream) {
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+           const fa::FwdParams& p, int grid, cudaStream_t stream) {
   if (set_smem_attr<D, BF16>() != cudaSuccess) return FA_ERR_CUDA;
-  fa::fa_fwd_kernel<D, BF16><<<grid, fa::kThreads, fa::Smem<D>::kAlloc, stream>>>(tq, tk, tv, p);
+  fa::fa_fwd_kernel<D, BF16><<<grid, fa::kThreads, fa::Smem<D>::kAlloc, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -179,16 +179,17 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   p.status = ds->status;
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_bshd(&tq, q, bf16, B, Sq, Hq, D) || !encode_bshd(&tk, k, bf16, B, Sk, Hkv, D) ||
-      !encode_bshd(&tv, v, bf16, B, Sk, Hkv, D))
+      !encode_bshd(&tv, v, bf16, B, Sk, Hkv, D) || !encode_bshd(&to, o, bf16, B, Sq, Hq, D, 32))
     return FA_ERR_CUDA;
 
   const int grid = static_cast<int>(std::min<long long>(items, ds->num_sms));
   if (D == 128) {
-    return bf16 ? launch<128, true>(tq, tk, tv, p, grid, stream) : launch<128, false>(tq, tk, tv, p, grid, stream);
+    return bf16 ? launch<128, true>(tq, tk, tv, to, p, grid, stream)
+                : launch<128, false>(tq, tk, tv, to, p, grid, stream);
   }
-  return bf16 ? launch<64, true>(tq, tk, tv, p, grid, stream) : launch<64, false>(tq, tk, tv, p, grid, stream);
+  return bf16 ? launch<64, true>(tq, tk, tv, to, p, grid, stream) : launch<64, false>(tq, tk, tv, to, p, grid, stream);
 }
 
 extern "C" int fa_status(fa_stream_t stream_) {

@@ -64,7 +64,11 @@ struct Smem {
   static constexpr int kStages = (D == 128) ? 4 : 6;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // O staging for the TMA store: one 64-column chunk (32 rows x 128 bytes per
+  // warp, 4 KB) per softmax warp, 8 warps.
+  static constexpr int kOStageOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kOStageWarpBytes = 32 * 128;
+  static constexpr int kBarOff = kOStageOff + 8 * kOStageWarpBytes;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_lo[2]
   //           p_hi[2] o_full[2] o_empty[2] teardown
   static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 2 + 1;
@@ -149,7 +153,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+              const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
   constexpr int kStages = L::kStages;
   constexpr uint32_t kTmemCols = 512;
@@ -201,6 +206,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     ptx::prefetch_tensormap(&tm_q);
     ptx::prefetch_tensormap(&tm_k);
     ptx::prefetch_tensormap(&tm_v);
+    ptx::prefetch_tensormap(&tm_o);
   }
   if (warp == kWarpMma) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -257,6 +263,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (w.n_kv == 0) continue;
       ok = load_q(0, w.hq0, w.r0, w.b) && load_kv(&tm_k, 0, w.kvh, w.b) && load_q(1, w.hq1, w.r1, w.b) &&
            load_kv(&tm_v, 0, w.kvh, w.b);
+      // Q tiles are read once from HBM: pull the next item's into L2 now so
+      // that its TMA load at the item boundary hits L2.
+      if (ok && lane == 0) {
+        const int nidx = item_of_round(round + 1, cta, grid);
+        if ((round + 1) * grid < p.n_items && nidx < p.n_items) {
+          const WorkItem nw = decode_item(p, nidx);
+          if (nw.n_kv > 0) {
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c) {
+              ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq0, nw.r0, nw.b);
+              ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq1, nw.r1, nw.b);
+            }
+          }
+        }
+      }
       for (int j = 1; ok && j < w.n_kv; ++j)
         ok = load_kv(&tm_k, j, w.kvh, w.b) && load_kv(&tm_v, j, w.kvh, w.b);
       ++act;
@@ -567,23 +588,45 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_arrive(bar_o_empty + 8 * t);
       const bool live = l_exact > 0.0f;
       const float inv_l = live ? __frcp_rn(l_exact + l_corr) : 0.0f;
-      if (row_valid) {
+      // Scale, round to the dtype and stage this warp's 32 rows one 64-column
+      // chunk at a time in the 128-byte-swizzled layout of the O tensor map;
+      // lane 0 stores each chunk with TMA (rows past Sq are clipped by it).
+      {
+        const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
+        const int wrow = row & 31;
+        const uint32_t stage = base + L::kOStageOff + warp * L::kOStageWarpBytes;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          uint4 v;
-          v.x = pack2<BF16>(__uint_as_float(orr[8 * c + 0]) * inv_l, __uint_as_float(orr[8 * c + 1]) * inv_l);
-          v.y = pack2<BF16>(__uint_as_float(orr[8 * c + 2]) * inv_l, __uint_as_float(orr[8 * c + 3]) * inv_l);
-          v.z = pack2<BF16>(__uint_as_float(orr[8 * c + 4]) * inv_l, __uint_as_float(orr[8 * c + 5]) * inv_l);
-          v.w = pack2<BF16>(__uint_as_float(orr[8 * c + 6]) * inv_l, __uint_as_float(orr[8 * c + 7]) * inv_l);
-          reinterpret_cast<uint4*>(orow)[c] = v;
+        for (int ch = 0; ch < L::kChunks; ++ch) {
+          uint32_t ob[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            float a0, a1;
+            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(orr[64 * ch + 2 * c]),
+                                                    __uint_as_float(orr[64 * ch + 2 * c + 1])), il2), a0, a1);
+            ob[c] = pack2<BF16>(a0, a1);
+          }
+          if (lane == 0) ptx::bulk_wait_group_read0();   // the previous store has read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            ptx::st_shared_v4(stage + wrow * 128 + ((k ^ (wrow & 7)) << 4), ob[4 * k], ob[4 * k + 1], ob[4 * k + 2],
+                              ob[4 * k + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_4d(&tm_o, stage, ch * 64, hq, r0 + (warp & 3) * 32, w.b);
+            ptx::bulk_commit_group();
+          }
         }
-        if (p.lse) {
-          const float lse = live ? (m_ref + __log2f(l_exact)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
-          p.lse[(static_cast<long long>(w.b) * p.Hq + hq) * p.Sq + i] = lse;
-        }
+      }
+      if (row_valid && p.lse) {
+        const float lse = live ? (m_ref + __log2f(l_exact)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
+        p.lse[(static_cast<long long>(w.b) * p.Hq + hq) * p.Sq + i] = lse;
       }
       ++act;
     }
+    if (lane == 0) ptx::bulk_wait_group0();   // every O store of this warp has completed
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
