@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     FAError,
     fa_debug_set_fault,
     fa_fwd,
+    fa_fwd_strided,
     fa_status,
     fa_status_string,
     fa_version,

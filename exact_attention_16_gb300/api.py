@@ -19,6 +19,7 @@ __all__ = [
     "lib",
     "library_path",
     "fa_fwd",
+    "fa_fwd_strided",
     "fa_status",
     "fa_status_string",
     "fa_version",
@@ -40,6 +41,12 @@ EXPORTED_SYMBOLS = {
                               ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                               ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                               ctypes.c_void_p]),
+    "fa_fwd_strided": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong),
+                                      ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
+                                      ctypes.POINTER(ctypes.c_longlong), ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p]),
     "fa_status": (ctypes.c_int, [ctypes.c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_version": (ctypes.c_int, []),
@@ -94,15 +101,21 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype}; expected torch.bfloat16 or torch.float16")
 
 
+def _bsh_strides(t):
+    return (ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
 def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=True, stream=None):
     """Attention forward: returns (O, LSE) (LSE is None if return_lse is False
     and no ``lse`` buffer is given).
 
-    q: (B, Sq, Hq, D); k, v: (B, Sk, Hkv, D); all contiguous CUDA tensors of
-    one 16-bit dtype on one device. ``scale`` defaults to 1/sqrt(D). ``causal``
-    selects the bottom-right aligned mask (query i sees key j iff
-    j <= i + Sk - Sq). ``out`` / ``lse`` may be preallocated (B, Sq, Hq, D)
-    and (B, Hq, Sq) float32 tensors.
+    q: (B, Sq, Hq, D); k, v: (B, Sk, Hkv, D) CUDA tensors of one 16-bit dtype
+    on one device, indexed (batch, seq, head, d). Any strides are accepted as
+    long as d is contiguous and the other strides are multiples of 8
+    elements (so ``x.transpose(1, 2)`` of a (B, H, S, D) tensor works as is).
+    ``scale`` defaults to 1/sqrt(D). ``causal`` selects the bottom-right
+    aligned mask (query i sees key j iff j <= i + Sk - Sq). ``out`` (any
+    such strides) and ``lse`` (contiguous (B, Hq, Sq) float32) may be given.
     """
     import torch
 
@@ -111,8 +124,8 @@ def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=
             raise TypeError(f"{name} must be a CUDA tensor")
         if t.dim() != 4:
             raise ValueError(f"{name} must be 4-D (batch, seq, heads, head_dim)")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
+        if t.stride(3) != 1:
+            raise ValueError(f"{name}: the head dimension must be contiguous")
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k and v must share one dtype")
     if not (q.device == k.device == v.device):
@@ -125,22 +138,26 @@ def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty_like(q)
-    elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor like q")
+        out = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device)
+    elif tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype or out.device != q.device or out.stride(3) != 1:
+        raise ValueError("out must be a (B, Sq, Hq, D) tensor like q with a contiguous head dimension")
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     elif lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32
                               or lse.device != q.device or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous float32 (B, Hq, Sq) tensor on q's device")
     with torch.cuda.device(q.device):
-        rc = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                          lse.data_ptr() if lse is not None else None,
-                          B, Sq, Sk, Hq, Hkv, D, float(scale), int(bool(causal)), code,
-                          _stream_handle(stream))
+        rc = lib().fa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None,
+                                  B, Sq, Sk, Hq, Hkv, D, _bsh_strides(q), _bsh_strides(k), _bsh_strides(v),
+                                  _bsh_strides(out), float(scale), int(bool(causal)), code,
+                                  _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
     return out, lse
+
+
+fa_fwd_strided = fa_fwd
 
 
 def fa_status(stream=None) -> int:

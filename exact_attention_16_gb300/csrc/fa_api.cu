@@ -18,11 +18,16 @@ namespace {
 
 __device__ int g_fa_status = 0;
 
-// Sk == 0: no key is visible, so O = 0 and LSE = -inf for every row.
-__global__ void fa_fill_empty_kernel(uint4* o, long long o_vec, float* lse, long long n_lse) {
+// Sk == 0: no key is visible, so O = 0 and LSE = -inf for every row. O rows
+// are (b, s, h) with element strides sb, ss, sh; each row is vec16 x 16 bytes.
+__global__ void fa_fill_empty_kernel(uint4* o, long long rows, int vec16, int Sq, int Hq, long long sb, long long ss,
+                                     long long sh, float* lse, long long n_lse) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < o_vec; i += stride)
-    o[i] = make_uint4(0, 0, 0, 0);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < rows * vec16; i += stride) {
+    const long long r = i / vec16, c = i % vec16;
+    const long long h = r % Hq, s = (r / Hq) % Sq, b = r / (static_cast<long long>(Hq) * Sq);
+    o[(b * sb + s * ss + h * sh) / 8 + c] = make_uint4(0, 0, 0, 0);
+  }
   if (lse)
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_lse; i += stride)
       lse[i] = -__int_as_float(0x7f800000);
@@ -90,13 +95,15 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // 4-D map over a (B, S, H, D) tensor: dims innermost first (D, H, S, B); the
 // box is 64 elements (128 bytes) x 1 head x `box_rows` rows x 1 batch,
 // 128-byte swizzle, zero fill outside the tensor (loads) / clipping (stores).
-bool encode_bshd(CUtensorMap* map, const void* ptr, bool bf16, int B, int S, int H, int D, int box_rows = 128) {
+bool encode_bshd(CUtensorMap* map, const void* ptr, bool bf16, int B, int S, int H, int D, const long long* st,
+                 int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                               static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
-                                 static_cast<cuuint64_t>(S) * H * D * 2};
+  // st = element strides of (b, s, h); the map wants byte strides of (h, s, b)
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
+                                 static_cast<cuuint64_t>(st[0]) * 2};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -126,8 +133,27 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
 
 }  // namespace
 
-extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
-                      int Hq, int Hkv, int D, float scale, int causal, int dtype, fa_stream_t stream_) {
+namespace {
+
+// Checks one tensor's (b, s, h) element strides (d is contiguous) and
+// replaces strides of size-1 dimensions, which are never used, by the
+// contiguous ones so that the tensor map accepts them.
+bool normalise_strides(const long long* in, long long* out, int B, int S, int H, int D) {
+  const long long natural[3] = {static_cast<long long>(S) * H * D, static_cast<long long>(H) * D, D};
+  const int sizes[3] = {B, S, H};
+  for (int a = 0; a < 3; ++a) {
+    long long st = in[a];
+    if (sizes[a] <= 1) st = natural[a];
+    if (st <= 0 || st % 8 != 0) return false;                  // 16-byte multiples for the tensor map
+    if (static_cast<double>(st) * 2.0 >= 1099511627776.0) return false;
+    out[a] = st;
+  }
+  return true;
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk, int Hq,
+             int Hkv, int D, const long long* qs_in, const long long* ks_in, const long long* vs_in,
+             const long long* os_in, float scale, int causal, int dtype, fa_stream_t stream_) {
   // ---- validation (nothing is enqueued on failure)
   if (B < 0 || Sq < 0 || Sk < 0 || Hq < 0 || Hkv < 0 || D < 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
@@ -140,23 +166,29 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   if (!aligned(q, 16) || !aligned(o, 16) || (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))) ||
       (lse && !aligned(lse, 4)))
     return FA_ERR_INVALID_ARG;
-  // the largest byte stride a tensor map may carry is below 2^40
-  const double q_bytes = static_cast<double>(Sq) * Hq * D * 2, kv_bytes = static_cast<double>(Sk) * Hkv * D * 2;
-  if (q_bytes >= 1099511627776.0 || kv_bytes >= 1099511627776.0) return FA_ERR_UNSUPPORTED;
+  long long qs[3], ks[3], vs[3], os[3];
+  if (!normalise_strides(qs_in, qs, B, Sq, Hq, D) || !normalise_strides(os_in, os, B, Sq, Hq, D))
+    return FA_ERR_INVALID_ARG;
+  if (Sk > 0 && (!normalise_strides(ks_in, ks, B, Sk, Hkv, D) || !normalise_strides(vs_in, vs, B, Sk, Hkv, D)))
+    return FA_ERR_INVALID_ARG;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   DeviceState* ds = device_state(nullptr);
   if (!ds) return FA_ERR_CUDA;
 
   if (Sk == 0) {
-    const long long o_vec = static_cast<long long>(B) * Sq * Hq * D * 2 / 16;
+    const long long rows = static_cast<long long>(B) * Sq * Hq;
     const long long n_lse = static_cast<long long>(B) * Hq * Sq;
-    fa_fill_empty_kernel<<<ds->num_sms * 4, 256, 0, stream>>>(static_cast<uint4*>(o), o_vec, lse, n_lse);
+    fa_fill_empty_kernel<<<ds->num_sms * 4, 256, 0, stream>>>(static_cast<uint4*>(o), rows, D / 8, Sq, Hq, os[0],
+                                                                os[1], os[2], lse, n_lse);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
 
   fa::FwdParams p{};
   p.o = o;
+  p.o_sb = os[0];
+  p.o_ss = os[1];
+  p.o_sh = os[2];
   p.lse = lse;
   p.B = B;
   p.Sq = Sq;
@@ -180,8 +212,8 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
   CUtensorMap tq, tk, tv, to;
-  if (!encode_bshd(&tq, q, bf16, B, Sq, Hq, D) || !encode_bshd(&tk, k, bf16, B, Sk, Hkv, D) ||
-      !encode_bshd(&tv, v, bf16, B, Sk, Hkv, D) || !encode_bshd(&to, o, bf16, B, Sq, Hq, D, 32))
+  if (!encode_bshd(&tq, q, bf16, B, Sq, Hq, D, qs) || !encode_bshd(&tk, k, bf16, B, Sk, Hkv, D, ks) ||
+      !encode_bshd(&tv, v, bf16, B, Sk, Hkv, D, vs) || !encode_bshd(&to, o, bf16, B, Sq, Hq, D, os, 32))
     return FA_ERR_CUDA;
 
   const int grid = static_cast<int>(std::min<long long>(items, ds->num_sms));
@@ -190,6 +222,25 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
                 : launch<128, false>(tq, tk, tv, to, p, grid, stream);
   }
   return bf16 ? launch<64, true>(tq, tk, tv, to, p, grid, stream) : launch<64, false>(tq, tk, tv, to, p, grid, stream);
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
+                      int Hq, int Hkv, int D, float scale, int causal, int dtype, fa_stream_t stream) {
+  const long long sq[3] = {static_cast<long long>(Sq) * Hq * D, static_cast<long long>(Hq) * D, D};
+  const long long skv[3] = {static_cast<long long>(Sk) * Hkv * D, static_cast<long long>(Hkv) * D, D};
+  return fwd_impl(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, sq, skv, skv, sq, scale, causal, dtype, stream);
+}
+
+extern "C" int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq,
+                              int Sk, int Hq, int Hkv, int D, const long long* q_strides,
+                              const long long* k_strides, const long long* v_strides,
+                              const long long* o_strides, float scale, int causal, int dtype,
+                              fa_stream_t stream) {
+  if (!q_strides || !k_strides || !v_strides || !o_strides) return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, q_strides, k_strides, v_strides, o_strides, scale, causal,
+                  dtype, stream);
 }
 
 extern "C" int fa_status(fa_stream_t stream_) {

@@ -40,8 +40,9 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 enum : int { kStatusOk = 0, kStatusTimeout = 4 };
 
 struct FwdParams {
-  void* o;               // (B, Sq, Hq, D) 16-bit
-  float* lse;            // (B, Hq, Sq) fp32 natural log, may be null
+  void* o;               // (B, Sq, Hq, D) 16-bit, element strides below, d contiguous
+  long long o_sb, o_ss, o_sh;
+  float* lse;            // (B, Hq, Sq) fp32 natural log, contiguous, may be null
   int B, Sq, Sk, Hq, Hkv, group;
   int causal;
   float scale_log2;      // softmax scale * log2(e)
@@ -440,7 +441,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int i = r0 + row;                // query row index
       const bool row_valid = i < p.Sq;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                      ((static_cast<long long>(w.b) * p.Sq + i) * p.Hq + hq) * (long long)D * 2;
+                      (static_cast<long long>(w.b) * p.o_sb + static_cast<long long>(i) * p.o_ss +
+                       static_cast<long long>(hq) * p.o_sh) * 2;
       if (w.n_kv == 0) {
         if (row_valid) {
           uint4 z = make_uint4(0, 0, 0, 0);

@@ -76,6 +76,22 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int Hkv, int D, float scale, int causal, int dtype, fa_stream_t stream);
 
 /*
+ * fa_fwd_strided — fa_fwd on strided tensors (e.g. the (B, H, S, D) layout of
+ * "NVIDIA闪存注意力实操" or views into a packed QKV buffer). Each tensor keeps
+ * its logical (batch, seq, head, d) indexing; `*_strides` point to three
+ * int64 element strides for (batch, seq, head), the head dimension d being
+ * contiguous. Strides of dimensions of size > 1 must be positive multiples
+ * of 8 elements (16 bytes) and below 2^39 elements; strides of size-1
+ * dimensions are ignored. lse stays (B, Hq, Sq) contiguous. Arguments and
+ * errors are otherwise those of fa_fwd; NULL stride pointers or invalid
+ * strides give FA_ERR_INVALID_ARG. Overlapping o with q, k or v is undefined.
+ */
+int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
+                   int Hq, int Hkv, int D, const long long* q_strides, const long long* k_strides,
+                   const long long* v_strides, const long long* o_strides, float scale, int causal, int dtype,
+                   fa_stream_t stream);
+
+/*
  * fa_status — synchronise `stream`, then read and clear the device status
  * word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's bounded
  * wait on an mbarrier ran out (the kernel then released its tensor memory

@@ -89,3 +89,33 @@ def test_sk_zero_needs_no_kv_pointers_but_still_validates(lib):
 def test_debug_fault_hook_validates(lib):
     assert api.fa_debug_set_fault(-2) == api.FA_ERR_INVALID_ARG
     assert api.fa_debug_set_fault(-1) == api.FA_OK
+
+
+def _call_strided(lib, qs=None, ks=None, vs=None, os_=None, **kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=None, B=2, Sq=4, Sk=4, Hq=2, Hkv=1, D=128,
+                scale=0.125, causal=0, dtype=1, stream=None)
+    args.update(kw)
+    arr = lambda x: None if x is None else (ctypes.c_longlong * 3)(*x)
+    nat_q = (args["Sq"] * args["Hq"] * 128, args["Hq"] * 128, 128)
+    nat_k = (args["Sk"] * args["Hkv"] * 128, args["Hkv"] * 128, 128)
+    return lib.fa_fwd_strided(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["Sq"],
+                              args["Sk"], args["Hq"], args["Hkv"], args["D"],
+                              arr(nat_q if qs is None else qs), arr(nat_k if ks is None else ks),
+                              arr(nat_k if vs is None else vs), arr(nat_q if os_ is None else os_),
+                              ctypes.c_float(args["scale"]), args["causal"], args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(qs=(1024, 256, 100)), api.FA_ERR_INVALID_ARG),     # head stride not a 16-byte multiple
+    (dict(ks=(0, 128, 128)), api.FA_ERR_INVALID_ARG),        # zero batch stride with B > 1
+    (dict(os_=(1024, -256, 128)), api.FA_ERR_INVALID_ARG),   # negative stride
+    (dict(B=0), api.FA_OK),
+])
+def test_strided_entry_validates_strides(lib, kw, code):
+    assert _call_strided(lib, **kw) == code
+
+
+def test_strided_entry_rejects_null_strides(lib):
+    rc = lib.fa_fwd_strided(16, 16, 16, 16, None, 1, 4, 4, 2, 1, 128, None, None, None, None,
+                            ctypes.c_float(0.125), 0, 1, None)
+    assert rc == api.FA_ERR_INVALID_ARG

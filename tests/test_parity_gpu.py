@@ -102,3 +102,40 @@ def test_repeatable_and_stream_ordered():
         o2, l2 = api.fa_fwd(q, k, v, causal=True)
     s.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def _oracle_compare(q, k, v, o, lse, scale, causal):
+    import oracle
+    from parity import compare
+    o_ref, l_ref = oracle.attention(q.float().cpu().numpy(), k.float().cpu().numpy(), v.float().cpu().numpy(),
+                                    scale, causal)
+    return compare(o.float().cpu().numpy().transpose(0, 2, 1, 3), lse.cpu().numpy(),
+                   o_ref.transpose(0, 2, 1, 3), l_ref)
+
+
+def test_bhsd_layout_with_strided_output():
+    """(B, H, S, D) storage passed as transposed views, O written into a
+    (B, H, S, D) buffer through its transposed view."""
+    from exact_attention_16_gb300.workloads import draw_inputs
+    w = W(2, 300, 333, 8, 2, 128, causal=True, seed=11)
+    q, k, v = draw_inputs(w)
+    qb, kb, vb = (t.transpose(1, 2).contiguous().cuda() for t in (q, k, v))   # (B, H, S, D)
+    o_store = torch.full((w.B, w.Hq, w.Sq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o, lse = api.fa_fwd(qb.transpose(1, 2), kb.transpose(1, 2), vb.transpose(1, 2), scale=w.scale, causal=True,
+                        out=o_store.transpose(1, 2))
+    assert api.fa_status() == 0
+    assert o.data_ptr() == o_store.data_ptr()
+    _oracle_compare(q, k, v, o, lse, w.scale, True)
+
+
+def test_packed_qkv_views():
+    """Q, K, V as views into one (B, S, 3, H, D) buffer (MHA), D = 64."""
+    g = torch.Generator().manual_seed(12)
+    B, S, H, D = 2, 257, 4, 64
+    qkv = (torch.randn(B, S, 3, H, D, generator=g)).to(torch.float16)
+    qkv_d = qkv.cuda()
+    q, k, v = qkv_d[:, :, 0], qkv_d[:, :, 1], qkv_d[:, :, 2]
+    assert not q.is_contiguous()
+    o, lse = api.fa_fwd(q, k, v, causal=False)
+    assert api.fa_status() == 0
+    _oracle_compare(qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2], o, lse, D ** -0.5, False)
