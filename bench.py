@@ -294,6 +294,65 @@ def run_ours(args, w):
     return rank, result
 
 
+def run_merge(args, w):
+    """Merge of `args.parts` partial (O, LSE) states shaped like the
+    workload's output (the exchange step of a context-parallel run):
+    HBM-bound, reported in GB/s of algorithmic bytes."""
+    import torch
+
+    from exact_attention_16_gb300 import api
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n = args.parts
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[w.dtype]
+    o_parts = torch.randn((n, w.B, w.Sq, w.Hq, w.D), generator=g, device=dev).to(dt)
+    lse_parts = torch.randn((n, w.B, w.Hq, w.Sq), generator=g, device=dev) * 3
+    out = torch.empty((w.B, w.Sq, w.Hq, w.D), dtype=dt, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    rows = w.B * w.Sq * w.Hq
+    nbytes = n * rows * w.D * 2 + n * rows * 4 + rows * w.D * 2 + rows * 4
+
+    def step():
+        api.fa_merge(o_parts, lse_parts, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stream = torch.cuda.current_stream(dev)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    launch_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    peaks = measured_peaks()
+    avg = sum(launch_ms) / len(launch_ms)
+    value = nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    return rank, {
+        "metric": "attention partial-state merge GB/s (algorithmic bytes)",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded torch normal draws)",
+        "config": {"workload": f"merge {n} parts shaped like {w.name}", "parts": n, "B": w.B, "Sq": w.Sq,
+                   "Hq": w.Hq, "D": w.D, "bytes_per_step": nbytes,
+                   "l2": f"inputs {nbytes >> 20} MiB > 129 MB L2; no flush"},
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / (avg * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(nbytes / (avg * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"] + " copy bandwidth", "traffic": None, "kernel": "merge_kernel",
+                     "avg_launch_ms": round(avg, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def oracle_sample(w, q32, k32, v32, rows_per_head: int, n_heads: int):
     """Time the oracle on the last `rows_per_head` rows of the first heads;
     returns (seconds, flops done)."""
@@ -384,6 +443,9 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["fwd", "merge"], default="fwd",
+                    help="fwd: the attention forward (default); merge: partial-state merge")
+    ap.add_argument("--parts", type=int, default=4, help="partial states for --op merge")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[x.name for x in WORKLOADS])
     ap.add_argument("--cpu-budget", type=float, default=18.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -393,6 +455,8 @@ def main():
     w = by_name(args.workload)
     if args.impl == "reference":
         rank, res = run_reference(args, w)
+    elif args.op == "merge":
+        rank, res = run_merge(args, w)
     else:
         rank, res = run_ours(args, w)
     if rank == 0 and res is not None:

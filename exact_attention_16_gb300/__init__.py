@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     fa_debug_set_fault,
     fa_fwd,
     fa_fwd_strided,
+    fa_merge,
     fa_status,
     fa_status_string,
     fa_version,

@@ -20,6 +20,7 @@ __all__ = [
     "library_path",
     "fa_fwd",
     "fa_fwd_strided",
+    "fa_merge",
     "fa_status",
     "fa_status_string",
     "fa_version",
@@ -47,6 +48,8 @@ EXPORTED_SYMBOLS = {
                                       ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
                                       ctypes.POINTER(ctypes.c_longlong), ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_void_p]),
+    "fa_merge": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fa_status": (ctypes.c_int, [ctypes.c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_version": (ctypes.c_int, []),
@@ -158,6 +161,35 @@ def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=
 
 
 fa_fwd_strided = fa_fwd
+
+
+def fa_merge(o_parts, lse_parts, *, out=None, lse=None, return_lse=True, stream=None):
+    """Merge partial attention results over disjoint key sets.
+
+    o_parts: (n, B, Sq, Hq, D) contiguous 16-bit CUDA tensor; lse_parts:
+    (n, B, Hq, Sq) contiguous float32. Returns (O, LSE) like fa_fwd.
+    """
+    import torch
+
+    if o_parts.dim() != 5 or lse_parts.dim() != 4:
+        raise ValueError("o_parts must be (n, B, Sq, Hq, D) and lse_parts (n, B, Hq, Sq)")
+    n, B, Sq, Hq, D = o_parts.shape
+    if tuple(lse_parts.shape) != (n, B, Hq, Sq) or lse_parts.dtype != torch.float32:
+        raise ValueError("lse_parts must be float32 (n, B, Hq, Sq)")
+    if not (o_parts.is_cuda and lse_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("o_parts and lse_parts must be contiguous CUDA tensors")
+    code = _dtype_code(o_parts)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=o_parts.dtype, device=o_parts.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        rc = lib().fa_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, Sq, Hq, D, code,
+                            _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_merge")
+    return out, lse
 
 
 def fa_status(stream=None) -> int:

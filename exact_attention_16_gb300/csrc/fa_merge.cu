@@ -1,0 +1,194 @@
+// Merge of attention outputs computed over disjoint key sets (context-parallel
+// shards or split-KV partials): LSE = ln sum_r e^{LSE_r}, O = sum_r
+// e^{LSE_r - LSE} O_r. This is the online-softmax rescale of "MiniPaged-Qwen:
+// Qwen3 Prefill FlashAttention" section 4 applied to whole partial states.
+// Memory bound: each thread folds eight elements of one row over the parts
+// with 16-byte streaming loads and fp32 accumulation.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/fa.h"
+#include "fa_merge.cuh"
+
+namespace fa {
+namespace {
+
+// Raw 16-byte chunks of a part and their conversion to fp32 (eight 16-bit
+// elements, or four fp32 elements, per chunk).
+template <typename T>
+struct Chunk {
+  static constexpr int kElems = 16 / sizeof(T);
+  __device__ static uint4 load(const T* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+  __device__ static void to_float(const uint4& v, float* x);
+};
+template <>
+__device__ void Chunk<float>::to_float(const uint4& v, float* x) {
+  x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y); x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+}
+template <>
+__device__ void Chunk<__nv_bfloat16>::to_float(const uint4& v, float* x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    x[2 * q] = __uint_as_float(w[q] << 16);
+    x[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+  }
+}
+template <>
+__device__ void Chunk<__half>::to_float(const uint4& v, float* x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+    x[2 * q] = f.x;
+    x[2 * q + 1] = f.y;
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if constexpr (BF16) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
+      w[q] = *reinterpret_cast<const uint32_t*>(&a);
+    } else {
+      const __half2 a = __floats2half2_rn(x[2 * q], x[2 * q + 1]);
+      w[q] = *reinterpret_cast<const uint32_t*>(&a);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+
+// o_parts: (n, B, Sq, Hq, D) of TP; lse_parts: (n, B, Hq, Sq) fp32;
+// o: (B, Sq, Hq, D) 16-bit; lse: (B, Hq, Sq) fp32 or null. Each thread owns
+// eight consecutive elements of one row and folds the parts in groups of
+// kGroup with a running max (the online-softmax rescale).
+template <typename TP, bool OUT_BF16, typename IDX>
+__global__ void __launch_bounds__(256, 3) merge_kernel(const TP* __restrict__ o_parts,
+                                                       const float* __restrict__ lse_parts, int n_parts,
+                                                       void* __restrict__ o, float* __restrict__ lse, IDX rows, IDX Sq,
+                                                       IDX Hq, IDX D) {
+  constexpr int kE = 16;                                   // output elements per thread
+  constexpr int kGroup = sizeof(TP) == 4 ? 2 : 4;          // parts whose loads are in flight together
+  constexpr int kChunks = kE / Chunk<TP>::kElems;           // 16-byte loads per part
+  const IDX per_row = D / kE;
+  const IDX items = rows * per_row;
+  const long long part_o = static_cast<long long>(rows) * D;
+  const IDX stride = static_cast<IDX>(gridDim.x) * blockDim.x;
+  for (IDX it = blockIdx.x * static_cast<IDX>(blockDim.x) + threadIdx.x; it < items; it += stride) {
+    const IDX row = it / per_row;
+    const IDX e = (it - row * per_row) * kE;
+    const IDX bs = row / Hq, h = row - bs * Hq;        // row = (b * Sq + s) * Hq + h
+    const IDX b = bs / Sq, s = bs - b * Sq;
+    const IDX li = (b * Hq + h) * Sq + s;
+    float m = -INFINITY, tot = 0.0f, acc[kE];
+#pragma unroll
+    for (int q = 0; q < kE; ++q) acc[q] = 0.0f;
+    for (int r0 = 0; r0 < n_parts; r0 += kGroup) {
+      float lr[kGroup];
+      uint4 raw[kGroup][kChunks];
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const int r = r0 + g;
+        lr[g] = (r < n_parts) ? __ldg(lse_parts + static_cast<long long>(r) * rows + li) : -INFINITY;
+        const TP* src = o_parts + r * part_o + static_cast<long long>(row) * D + e;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+          raw[g][c] = (r < n_parts) ? Chunk<TP>::load(src + c * Chunk<TP>::kElems) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        if (!(lr[g] > -INFINITY)) continue;
+        const float m_new = fmaxf(m, lr[g]);
+        const float c = expf(m - m_new);          // 0 while m = -inf
+        const float wgt = expf(lr[g] - m_new);
+        tot = tot * c + wgt;
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch) {
+          float x[Chunk<TP>::kElems];
+          Chunk<TP>::to_float(raw[g][ch], x);
+#pragma unroll
+          for (int q = 0; q < Chunk<TP>::kElems; ++q) {
+            float& a = acc[ch * Chunk<TP>::kElems + q];
+            a = fmaf(wgt, x[q], a * c);
+          }
+        }
+        m = m_new;
+      }
+    }
+    const bool live = m > -INFINITY;
+    const float inv = live ? 1.0f / tot : 0.0f;
+#pragma unroll
+    for (int q = 0; q < kE; ++q) acc[q] *= inv;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(o) + static_cast<long long>(row) * D + e);
+    float lo[8], hi[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      lo[q] = acc[q];
+      hi[q] = acc[8 + q];
+    }
+    __stcs(dst, pack8<OUT_BF16>(lo));
+    __stcs(dst + 1, pack8<OUT_BF16>(hi));
+    if (lse && e == 0) lse[li] = live ? m + logf(tot) : -INFINITY;
+  }
+}
+
+template <typename TP, bool OUT_BF16>
+int launch_merge(const TP* o_parts, const float* lse_parts, int n, void* o, float* lse, long long rows, int Sq,
+                 int Hq, int D, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return FA_ERR_CUDA;
+  const long long items = rows * (D / 16);
+  const long long blocks_needed = (items + 255) / 256;
+  const int blocks = static_cast<int>(blocks_needed < 32LL * sms ? blocks_needed : 32LL * sms);
+  if (items * 8 + 256LL * blocks < 0x7fffffffLL)   // every index (and the loop bound) fits 32 bits
+    merge_kernel<TP, OUT_BF16, unsigned><<<blocks, 256, 0, stream>>>(
+        o_parts, lse_parts, n, o, lse, static_cast<unsigned>(rows), static_cast<unsigned>(Sq),
+        static_cast<unsigned>(Hq), static_cast<unsigned>(D));
+  else
+    merge_kernel<TP, OUT_BF16, long long><<<blocks, 256, 0, stream>>>(o_parts, lse_parts, n, o, lse, rows, Sq, Hq, D);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+int merge_f32_parts(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int B, int Sq,
+                    int Hq, int D, int dtype, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(B) * Sq * Hq;
+  if (rows == 0) return FA_OK;
+  return dtype == FA_DTYPE_BF16 ? launch_merge<float, true>(o_parts, lse_parts, n_parts, o, lse, rows, Sq, Hq, D, stream)
+                                : launch_merge<float, false>(o_parts, lse_parts, n_parts, o, lse, rows, Sq, Hq, D,
+                                                             stream);
+}
+
+}  // namespace fa
+
+extern "C" int fa_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int B, int Sq,
+                        int Hq, int D, int dtype, fa_stream_t stream_) {
+  if (n_parts < 1 || B < 0 || Sq < 0 || Hq < 0 || D < 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (D % 16 != 0 || D > 1024) return FA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(B) * Sq * Hq;
+  if (rows == 0 || D == 0) return FA_OK;
+  if (!o_parts || !lse_parts || !o) return FA_ERR_INVALID_ARG;
+  if (!fa::aligned_to(o_parts, 16) || !fa::aligned_to(o, 16) || !fa::aligned_to(lse_parts, 4) ||
+      (lse && !fa::aligned_to(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dtype == FA_DTYPE_BF16)
+    return fa::launch_merge<__nv_bfloat16, true>(static_cast<const __nv_bfloat16*>(o_parts), lse_parts, n_parts, o,
+                                                 lse, rows, Sq, Hq, D, stream);
+  return fa::launch_merge<__half, false>(static_cast<const __half*>(o_parts), lse_parts, n_parts, o, lse, rows, Sq, Hq,
+                                         D, stream);
+}

@@ -92,6 +92,26 @@ int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* 
                    fa_stream_t stream);
 
 /*
+ * fa_merge — combine attention outputs computed over disjoint key sets (for
+ * example key shards of a context-parallel run, each produced by fa_fwd):
+ *     LSE = ln sum_r exp(LSE_r),   O = sum_r exp(LSE_r - LSE) O_r,
+ * the online-softmax rescale of "MiniPaged-Qwen: Qwen3 Prefill
+ * FlashAttention" section 4 applied to whole partial states.
+ * o_parts   device, (n_parts, B, Sq, Hq, D) contiguous, element type `dtype`
+ * lse_parts device, (n_parts, B, Hq, Sq) contiguous float32 (natural log);
+ *           a part with LSE_r = -inf holds no key for that row and is skipped
+ * o         device, (B, Sq, Hq, D) contiguous `dtype`, fully overwritten
+ * lse       device, (B, Hq, Sq) float32, or NULL. Rows where every part is
+ *           -inf get O = 0 and LSE = -inf.
+ * n_parts >= 1; D a multiple of 16, at most 1024. o_parts and o 16-byte
+ * aligned, lse arrays 4-byte aligned. Errors as for fa_fwd (FA_ERR_INVALID_ARG
+ * for bad sizes, pointers or dtype, FA_ERR_UNSUPPORTED for D). Asynchronous on
+ * `stream`; allocates nothing.
+ */
+int fa_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int B, int Sq, int Hq,
+             int D, int dtype, fa_stream_t stream);
+
+/*
  * fa_status — synchronise `stream`, then read and clear the device status
  * word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's bounded
  * wait on an mbarrier ran out (the kernel then released its tensor memory

@@ -16,6 +16,7 @@ from .exact import (  # noqa: F401
     attention_rows,
     attention_brute,
     attention_online,
+    merge_partials,
     probabilities,
     kv_head_of,
     visibility,

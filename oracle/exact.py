@@ -41,6 +41,7 @@ __all__ = [
     "probabilities",
     "attention_brute",
     "attention_online",
+    "merge_partials",
 ]
 
 
@@ -265,3 +266,35 @@ def attention_online(q, k, v, scale: float, causal: bool, block_n: int):
             with np.errstate(divide="ignore"):
                 lse[b, hq, :] = np.where(live, m_old + np.log(np.where(live, l_old, 1.0)), -np.inf)
     return o, lse
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention outputs computed over disjoint key sets.
+
+    o_parts: (n, B, Sq, Hq, D); lse_parts: (n, B, Hq, Sq) natural-log LSE of
+    each part. With m the running maximum and alpha the rescale factor of the
+    online-softmax recurrence ([MiniPaged-Qwen] section 4; [cuTile-FMHA]
+    "在线Softmax算法"), part r holds O_r = sum_j e^{s_j - LSE_r} v_j over its
+    keys, so the whole is
+
+        LSE = ln sum_r e^{LSE_r},    O = sum_r e^{LSE_r - LSE} O_r.
+
+    Parts with LSE_r = -inf (no visible key) contribute nothing; a row with
+    no part holding a key gets O = 0 and LSE = -inf. Returns float64 arrays.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    if o_parts.ndim != 5 or lse_parts.ndim != 4 or o_parts.shape[0] != lse_parts.shape[0]:
+        raise ValueError("o_parts must be (n, B, Sq, Hq, D) and lse_parts (n, B, Hq, Sq)")
+    n, B, Sq, Hq, D = o_parts.shape
+    lse_bshq = lse_parts.transpose(0, 1, 3, 2)                 # (n, B, Sq, Hq)
+    m = lse_bshq.max(axis=0)                                    # (B, Sq, Hq)
+    live = np.isfinite(m)
+    ref = np.where(live, m, 0.0)
+    w = np.exp(lse_bshq - ref[None])                            # 0 for -inf parts
+    tot = w.sum(axis=0)
+    with np.errstate(divide="ignore"):
+        lse = np.where(live, ref + np.log(np.where(live, tot, 1.0)), -np.inf)
+    o = (w[..., None] * o_parts).sum(axis=0) / np.where(live, tot, 1.0)[..., None]
+    o[~live] = 0.0
+    return o, lse.transpose(0, 2, 1)

@@ -119,3 +119,15 @@ def test_strided_entry_rejects_null_strides(lib):
     rc = lib.fa_fwd_strided(16, 16, 16, 16, None, 1, 4, 4, 2, 1, 128, None, None, None, None,
                             ctypes.c_float(0.125), 0, 1, None)
     assert rc == api.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,code", [
+    ((16, 16, 0, 16, None, 1, 4, 2, 128, 1), api.FA_ERR_INVALID_ARG),   # n_parts = 0
+    ((16, 16, 2, 16, None, 1, 4, 2, 124, 1), api.FA_ERR_UNSUPPORTED),   # D not a multiple of 16
+    ((16, 16, 2, 16, None, 1, 4, 2, 128, 3), api.FA_ERR_INVALID_ARG),   # dtype
+    ((None, 16, 2, 16, None, 1, 4, 2, 128, 1), api.FA_ERR_INVALID_ARG),
+    ((24, 16, 2, 16, None, 1, 4, 2, 128, 1), api.FA_ERR_INVALID_ARG),   # misaligned parts
+    ((16, 16, 2, 16, None, 0, 4, 2, 128, 1), api.FA_OK),                # nothing to merge
+])
+def test_merge_validates_before_any_launch(lib, args, code):
+    assert lib.fa_merge(*args, None) == code

@@ -346,3 +346,60 @@ def test_planted_mask_mistakes_are_caught(monkeypatch, kind):
         return j < rows[:, None] + (Sk - Sq)
     monkeypatch.setattr(oa, "visibility", vis)
     assert _pins_fail(None)
+
+
+# --------------------------------------------------------------------------
+# Merging partial (O, LSE) over key shards
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cuts", [(4,), (1, 6), (3, 5, 9)])
+def test_merge_of_key_shards_equals_attention_over_all_keys(cuts):
+    """Non-causal: attention over key shards [c_r, c_{r+1}) merged by LSE
+    equals attention over every key."""
+    B, Sq, Sk, Hq, Hkv, D = 2, 5, 11, 4, 2, 3
+    q, k, v = rand_qkv(13, B, Sq, Sk, Hq, Hkv, D, sigma=1.5)
+    o_full, l_full = oracle.attention(q, k, v, 0.6, causal=False)
+    edges = [0, *cuts, Sk]
+    parts = [oracle.attention(q, k[:, a:b], v[:, a:b], 0.6, causal=False) for a, b in zip(edges[:-1], edges[1:])]
+    o, l = oracle.merge_partials(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    np.testing.assert_allclose(o, o_full, atol=1e-12)
+    np.testing.assert_allclose(l, l_full, atol=1e-12)
+
+
+def test_merge_with_causal_suffix_shard():
+    """Causal, Sk >= Sq: keys [0, a) with a <= Sk - Sq + 1 are visible to every
+    query (non-causal shard); keys [a, Sk) keep the bottom-right mask of their
+    own lengths. Merging the two equals causal attention over all keys,
+    including rows that see nothing in the second shard."""
+    B, Sq, Sk, Hq, D = 1, 4, 9, 2, 3
+    q, k, v = rand_qkv(14, B, Sq, Sk, Hq, Hq, D)
+    o_full, l_full = oracle.attention(q, k, v, 0.9, causal=True)
+    a = Sk - Sq + 1
+    p0 = oracle.attention(q, k[:, :a], v[:, :a], 0.9, causal=False)
+    p1 = oracle.attention(q, k[:, a:], v[:, a:], 0.9, causal=True)
+    assert np.isinf(p1[1]).any()                     # row 0 sees no key of the suffix
+    o, l = oracle.merge_partials(np.stack([p0[0], p1[0]]), np.stack([p0[1], p1[1]]))
+    np.testing.assert_allclose(o, o_full, atol=1e-12)
+    np.testing.assert_allclose(l, l_full, atol=1e-12)
+
+
+def test_merge_all_empty_parts_and_single_part():
+    o_parts = np.random.default_rng(15).standard_normal((3, 1, 2, 2, 4))
+    lse = np.full((3, 1, 2, 2), -np.inf)
+    o, l = oracle.merge_partials(o_parts, lse)
+    assert np.all(o == 0) and np.all(l == -np.inf)
+    lse1 = np.random.default_rng(16).standard_normal((1, 1, 2, 2))
+    o1, l1 = oracle.merge_partials(o_parts[:1], lse1)
+    np.testing.assert_allclose(o1, o_parts[0], atol=1e-15)
+    np.testing.assert_allclose(l1, lse1[0], atol=1e-15)
+
+
+def test_planted_merge_mistake_is_caught(monkeypatch):
+    real = oa.merge_partials
+
+    def no_rescale(o_parts, lse_parts):        # plain average of the parts
+        o, l = real(o_parts, lse_parts)
+        return np.asarray(o_parts).mean(axis=0), l
+    monkeypatch.setattr(oracle, "merge_partials", no_rescale)
+    with pytest.raises(AssertionError):
+        test_merge_of_key_shards_equals_attention_over_all_keys((4,))
