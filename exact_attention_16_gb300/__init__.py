@@ -12,6 +12,8 @@ from .api import (  # noqa: F401
     fa_fwd,
     fa_fwd_strided,
     fa_merge,
+    fa_fwd_decode,
+    fa_decode_workspace_size,
     fa_status,
     fa_status_string,
     fa_version,

@@ -21,6 +21,8 @@ __all__ = [
     "fa_fwd",
     "fa_fwd_strided",
     "fa_merge",
+    "fa_fwd_decode",
+    "fa_decode_workspace_size",
     "fa_status",
     "fa_status_string",
     "fa_version",
@@ -50,6 +52,13 @@ EXPORTED_SYMBOLS = {
                                       ctypes.c_void_p]),
     "fa_merge": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "fa_fwd_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]),
+    "fa_decode_workspace_size": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_status": (ctypes.c_int, [ctypes.c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_version": (ctypes.c_int, []),
@@ -189,6 +198,57 @@ def fa_merge(o_parts, lse_parts, *, out=None, lse=None, return_lse=True, stream=
                             _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_merge")
+    return out, lse
+
+
+def fa_decode_workspace_size(B, Sq, Sk, Hq, Hkv, D, num_splits=0) -> int:
+    """Workspace bytes fa_fwd_decode needs on the current device."""
+    out = ctypes.c_ulonglong(0)
+    rc = lib().fa_decode_workspace_size(B, Sq, Sk, Hq, Hkv, D, num_splits, ctypes.byref(out))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_decode_workspace_size")
+    return int(out.value)
+
+
+def fa_fwd_decode(q, k, v, *, scale=None, causal=False, num_splits=0, workspace=None, out=None, lse=None,
+                  return_lse=True, stream=None):
+    """Split-KV attention for few query rows per KV head (decode).
+
+    Same tensors and result as fa_fwd (contiguous (B, S, H, D)); requires
+    (Hq / Hkv) * Sq <= 128. ``workspace`` is a CUDA uint8 tensor of at least
+    fa_decode_workspace_size(...) bytes; when omitted one is allocated here
+    (through torch's allocator) for this call.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    if not (q.dtype == k.dtype == v.dtype) or not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must share one dtype and device")
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be (B, Sk, Hkv, D) matching q")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        need = fa_decode_workspace_size(B, Sq, Sk, Hq, Hkv, D, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+        rc = lib().fa_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, B, Sq, Sk, Hq, Hkv, D, float(scale),
+                                 int(bool(causal)), code, int(num_splits),
+                                 workspace.data_ptr() if workspace is not None else None,
+                                 workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                                 _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_decode")
     return out, lse
 
 

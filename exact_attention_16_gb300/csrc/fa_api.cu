@@ -226,6 +226,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 }  // namespace
 
+namespace fa {
+int* current_status_word() {
+  DeviceState* ds = device_state(nullptr);
+  return ds ? ds->status : nullptr;
+}
+}  // namespace fa
+
 extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
                       int Hq, int Hkv, int D, float scale, int causal, int dtype, fa_stream_t stream) {
   const long long sq[3] = {static_cast<long long>(Sq) * Hq * D, static_cast<long long>(Hq) * D, D};

@@ -1,0 +1,171 @@
+// Host side of the split-KV path (fa_fwd_decode): argument checks, split
+// selection, tensor maps, launch of fa_decode_kernel and of the merge.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_decode_kernel.cuh"
+#include "fa_merge.cuh"
+#include "tma_host.h"
+
+namespace fa {
+int* current_status_word();   // fa_api.cu: the per-device status word read by fa_status()
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct Plan {
+  int n_tiles = 0, n_splits = 1, tiles_per_split = 0;
+  unsigned long long o_part_bytes = 0, lse_part_bytes = 0;
+  unsigned long long workspace_bytes() const { return n_splits > 1 ? o_part_bytes + lse_part_bytes : 0; }
+};
+
+int device_sms() {
+  static int sms[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (sms[dev] == 0) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev];
+}
+
+// Splits of the key range: the requested number, or (num_splits <= 0) enough
+// to give about two waves of CTAs on `sms` SMs; every split has >= 1 tile.
+Plan make_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int num_splits, int sms) {
+  Plan pl;
+  pl.n_tiles = (Sk + 127) / 128;
+  int want = num_splits;
+  if (want <= 0) {
+    const long long units = static_cast<long long>(B) * Hkv;
+    const long long target = 2LL * (sms > 0 ? sms : 148);
+    want = static_cast<int>(units >= target ? 1 : (target + units - 1) / units);
+  }
+  if (want > pl.n_tiles) want = pl.n_tiles;
+  if (want < 1) want = 1;
+  pl.tiles_per_split = pl.n_tiles > 0 ? (pl.n_tiles + want - 1) / want : 0;
+  pl.n_splits = pl.tiles_per_split > 0 ? (pl.n_tiles + pl.tiles_per_split - 1) / pl.tiles_per_split : 1;
+  const unsigned long long rows = static_cast<unsigned long long>(B) * Sq * Hq;
+  pl.o_part_bytes = static_cast<unsigned long long>(pl.n_splits) * rows * D * 4;
+  pl.lse_part_bytes = (static_cast<unsigned long long>(pl.n_splits) * rows * 4 + 15) / 16 * 16;
+  return pl;
+}
+
+// Checks shared by the size query and the launch (no device access).
+int check_args(int B, int Sq, int Sk, int Hq, int Hkv, int D, int dtype) {
+  if (B < 0 || Sq < 0 || Sk < 0 || Hq < 0 || Hkv < 0 || D < 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(Hq / Hkv) * Sq > 128) return FA_ERR_UNSUPPORTED;   // rows per KV head in one tile
+  return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+template <int D, bool BF16>
+int launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::DecodeParams& p,
+                  dim3 grid, cudaStream_t stream) {
+  static std::once_flag f[kMaxDevices];
+  static cudaError_t err[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::call_once(f[dev], [&] {
+    err[dev] = cudaFuncSetAttribute(fa::fa_decode_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    fa::DecodeSmem<D>::kAlloc);
+  });
+  if (err[dev] != cudaSuccess) return FA_ERR_CUDA;
+  fa::fa_decode_kernel<D, BF16><<<grid, 192, fa::DecodeSmem<D>::kAlloc, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+unsigned long long timeout_ns() {
+  static const unsigned long long ns = [] {
+    const char* e = std::getenv("FA_WAIT_TIMEOUT_MS");
+    const long long ms = e ? std::atoll(e) : 0;
+    return static_cast<unsigned long long>(ms > 0 ? ms : 2000) * 1000000ull;
+  }();
+  return ns;
+}
+
+}  // namespace
+
+namespace fa {
+
+// Launch on a given workspace (o_part / lse_part only read when n_splits > 1).
+int decode_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk, int Hq,
+                  int Hkv, int D, float scale, int causal, int dtype, int num_splits, float* o_part, float* lse_part,
+                  unsigned long long workspace_bytes, cudaStream_t stream, int* status_word) {
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const Plan pl = make_plan(B, Sq, Sk, Hq, Hkv, D, num_splits, device_sms());
+  if (pl.n_splits > 1 && (workspace_bytes < pl.workspace_bytes() || !o_part || !lse_part)) return FA_ERR_INVALID_ARG;
+  const long long sq[3] = {static_cast<long long>(Sq) * Hq * D, static_cast<long long>(Hq) * D, D};
+  const long long skv[3] = {static_cast<long long>(Sk) * Hkv * D, static_cast<long long>(Hkv) * D, D};
+  const int G = Hq / Hkv;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bshd_box(&tq, q, bf16, B, Sq, Hq, D, sq, G, Sq) ||
+      !encode_bshd_box(&tk, k, bf16, B, Sk, Hkv, D, skv, 1, 128) ||
+      !encode_bshd_box(&tv, v, bf16, B, Sk, Hkv, D, skv, 1, 128))
+    return FA_ERR_CUDA;
+  DecodeParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.R = G * Sq;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.n_splits = pl.n_splits;
+  p.tiles_per_split = pl.tiles_per_split;
+  p.n_kv_tiles = pl.n_tiles;
+  p.timeout_ns = timeout_ns();
+  p.status = status_word;
+  const dim3 grid(pl.n_splits, Hkv, B);
+  int rc = D == 128 ? (bf16 ? launch_decode<128, true>(tq, tk, tv, p, grid, stream)
+                            : launch_decode<128, false>(tq, tk, tv, p, grid, stream))
+                    : (bf16 ? launch_decode<64, true>(tq, tk, tv, p, grid, stream)
+                            : launch_decode<64, false>(tq, tk, tv, p, grid, stream));
+  if (rc != FA_OK || pl.n_splits == 1) return rc;
+  return merge_f32_parts(o_part, lse_part, pl.n_splits, o, lse, B, Sq, Hq, D, dtype, stream);
+}
+
+}  // namespace fa
+
+extern "C" int fa_decode_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D, int num_splits,
+                                        unsigned long long* bytes) {
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  const int rc = check_args(B, Sq, Sk, Hq, Hkv, D, FA_DTYPE_BF16);
+  if (rc != FA_OK || B == 0 || Sq == 0 || Hq == 0 || Sk == 0) return rc;
+  // the automatic split count depends on the SM count of the current device
+  *bytes = make_plan(B, Sq, Sk, Hq, Hkv, D, num_splits, num_splits > 0 ? 0 : device_sms()).workspace_bytes();
+  return FA_OK;
+}
+
+extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
+                             int Hq, int Hkv, int D, float scale, int causal, int dtype, int num_splits,
+                             void* workspace, unsigned long long workspace_bytes, fa_stream_t stream_) {
+  int rc = check_args(B, Sq, Sk, Hq, Hkv, D, dtype);
+  if (rc != FA_OK) return rc;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
+  if (Sk == 0) return fa_fwd(q, k, v, o, lse, B, Sq, 0, Hq, Hkv, D, scale, causal, dtype, stream_);
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
+      (workspace && !aligned(workspace, 16)))
+    return FA_ERR_INVALID_ARG;
+  int* status = fa::current_status_word();
+  if (!status) return FA_ERR_CUDA;
+  const Plan pl = make_plan(B, Sq, Sk, Hq, Hkv, D, num_splits, device_sms());
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.o_part_bytes) : nullptr;
+  return fa::decode_launch(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, dtype, num_splits, o_part,
+                           lse_part, workspace_bytes, reinterpret_cast<cudaStream_t>(stream_), status);
+}

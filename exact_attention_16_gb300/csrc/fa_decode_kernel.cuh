@@ -1,0 +1,386 @@
+// Split-KV attention for few query rows per KV head (decode and short
+// chunks), sm_103a. One CTA handles the G x Sq query rows that share one KV
+// head (GQA group x query positions, "MiniPaged-Qwen: Qwen3 Prefill
+// FlashAttention" section 6) against one contiguous range of 128-key tiles
+// (a split); the per-split results are normalised partial states (O_s,
+// LSE_s) that a merge combines, or the final O when there is one split.
+// Same arithmetic as the prefill kernel (online softmax with exp2 and the
+// log2e-folded scale, bottom-right causal limit of section 13): TMA K/V
+// ring, tcgen05 Q K^T into a double-buffered S in tensor memory, softmax by
+// one thread per row, P V with P read from tensor memory.
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue (TMEM lanes 0-127,
+// row r = s * G + g), warp 4 TMA producer, warp 5 MMA issuer / TMEM owner.
+// TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256, 256+D).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+struct DecodeParams {
+  void* o;             // final O (B, Sq, Hq, D) 16-bit (one split)
+  float* lse;          // final LSE (B, Hq, Sq) or null (one split)
+  float* o_part;       // (n_splits, B, Sq, Hq, D) fp32 partial O (several splits)
+  float* lse_part;     // (n_splits, B, Hq, Sq) fp32 partial LSE
+  int B, Sq, Sk, Hq, Hkv, G, R;    // R = G * Sq query rows per CTA (<= 128)
+  int causal;
+  float scale_log2;
+  int n_splits, tiles_per_split, n_kv_tiles;
+  unsigned long long timeout_ns;
+  int* status;
+};
+
+template <int D>
+struct DecodeSmem {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = (D == 128) ? 5 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full, pv_done, o_full, teardown
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 1 + 1 + 1 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kAlloc = kMiscOff + 16 + 1024;
+};
+
+__device__ __forceinline__ bool dec_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         const DecodeParams& p) {
+  if (ptx::mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+        atomicCAS(p.status, 0, 4);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t dec_pack2(float lo, float hi) {
+  if constexpr (BF16) return ptx::pack_bf16x2(lo, hi);
+  else return ptx::pack_f16x2(lo, hi);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(192, 1)
+fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ DecodeParams p) {
+  using L = DecodeSmem<D>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr float kRescale = 8.0f;
+  const float kNegInf = -__int_as_float(0x7f800000);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t sQ = base + L::kQOff;
+  const uint32_t sKV = base + L::kKVOff;
+  const uint32_t bar_q_full = base + L::kBarOff;
+  const uint32_t bar_kv_full = bar_q_full + 8;
+  const uint32_t bar_kv_empty = bar_kv_full + 8 * kStages;
+  const uint32_t bar_s_full = bar_kv_empty + 8 * kStages;   // [2]
+  const uint32_t bar_p_full = bar_s_full + 16;
+  const uint32_t bar_pv_done = bar_p_full + 8;
+  const uint32_t bar_o_full = bar_pv_done + 8;
+  const uint32_t bar_teardown = bar_o_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int t_begin = split * p.tiles_per_split;
+  const int t_end = min(p.n_kv_tiles, t_begin + p.tiles_per_split);
+  const int n = max(0, t_end - t_begin);
+
+  // Rows R..127 of the Q tile are never loaded: zero them so that the
+  // unused rows of S, P and O stay finite.
+  for (int i = threadIdx.x; i < L::kTileBytes / 16; i += blockDim.x) {
+    const int row = (i * 16 / 128) % 128;
+    if (row >= p.R) reinterpret_cast<uint4*>(base_ptr + L::kQOff)[i] = make_uint4(0, 0, 0, 0);
+  }
+  ptx::fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar_kv_full + 8 * s, 1);
+      ptx::mbar_init(bar_kv_empty + 8 * s, 1);
+    }
+    ptx::mbar_init(bar_s_full, 1);
+    ptx::mbar_init(bar_s_full + 8, 1);
+    ptx::mbar_init(bar_p_full, 128);
+    ptx::mbar_init(bar_pv_done, 1);
+    ptx::mbar_init(bar_o_full, 1);
+    ptx::mbar_init(bar_teardown, 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    uint32_t issued = 0;
+    if (n > 0 && lane == 0) {
+      const uint64_t pol_kv = ptx::policy_evict_first();   // each K/V byte is read once
+      const uint32_t q_bytes = static_cast<uint32_t>(p.R) * 128u * L::kChunks;
+      ptx::mbar_arrive_expect_tx(bar_q_full, q_bytes);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, 0, b, pol_kv);
+      for (int j = 0; ok && j < 2 * n; ++j) {               // K_0, V_0, K_1, V_1, ...
+        const uint32_t st = j % kStages, ph = ((j / kStages) & 1u) ^ 1u;
+        if (!(ok = dec_wait(bar_kv_empty + 8 * st, ph, abort_flag, p))) break;
+        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * st, L::kTileBytes);
+        const CUtensorMap* map = (j & 1) ? &tm_v : &tm_k;
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_4d(sKV + st * L::kTileBytes + c * L::kChunkBytes, map, bar_kv_full + 8 * st, c * 64, kvh,
+                           (t_begin + j / 2) * 128, b, pol_kv);
+        ++issued;
+      }
+      if (!ok) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        for (uint32_t k = (issued > (uint32_t)kStages ? issued - kStages : 0); k < issued; ++k)
+          while (!ptx::mbar_try_wait(bar_kv_full + 8 * (k % kStages), (k / kStages) & 1u) &&
+                 ptx::globaltimer_ns() - t0 < 2000000ull) {
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = ptx::idesc_f16(BF16, 128, 128, false, false);
+    constexpr uint32_t idesc_o = ptx::idesc_f16(BF16, 128, D, false, true);
+    const uint64_t dq = ptx::sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dk0 = ptx::sdesc_sw128(sKV, 16, 1024);
+    const uint64_t dv0 = ptx::sdesc_sw128(sKV, L::kChunkBytes, 1024);
+    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;
+    bool ok = true;
+    auto wait_load = [&](int j) -> bool {   // j-th load: K_{j/2} or V_{j/2}
+      return dec_wait(bar_kv_full + 8 * (j % kStages), (j / kStages) & 1u, abort_flag, p);
+    };
+    auto issue_s = [&](int jt) {            // S buffer jt%2 = Q K_jt^T
+      const uint32_t st = (2 * jt) % kStages;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = static_cast<uint32_t>(((ks / 4) * L::kChunkBytes + (ks % 4) * 32) >> 4);
+        ptx::mma_ss(tmem + 128 * (jt & 1), dq + off, dk0 + st * kStageDesc + off, idesc_s, ks > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar_s_full + 8 * (jt & 1));
+      ptx::mma_commit(bar_kv_empty + 8 * st);
+    };
+    if (n > 0) {
+      ok = dec_wait(bar_q_full, 0, abort_flag, p) && wait_load(0);
+      if (ok) {
+        ptx::tc_fence_after();
+        if (lane == 0) issue_s(0);
+        __syncwarp();
+      }
+      if (ok && n > 1 && (ok = wait_load(2))) {
+        ptx::tc_fence_after();
+        if (lane == 0) issue_s(1);
+        __syncwarp();
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        if (!(ok = dec_wait(bar_p_full, j & 1, abort_flag, p) && wait_load(2 * j + 1))) break;
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vst = (2 * j + 1) % kStages;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            ptx::mma_ts(tmem + 256, tmem + 128 * (j & 1) + ks * 8,
+                        dv0 + vst * kStageDesc + static_cast<uint32_t>((ks * 16 * 128) >> 4), idesc_o,
+                        (j == 0 && ks == 0) ? 0u : 1u);
+          ptx::mma_commit(bar_pv_done);
+          ptx::mma_commit(bar_kv_empty + 8 * vst);
+          if (j + 1 == n) ptx::mma_commit(bar_o_full);
+        }
+        __syncwarp();
+        if (j + 2 < n) {
+          if (!(ok = wait_load(2 * (j + 2)))) break;
+          ptx::tc_fence_after();
+          if (lane == 0) issue_s(j + 2);
+          __syncwarp();
+        }
+      }
+      if (!ok) {
+        if (lane == 0) ptx::mma_commit(bar_teardown);
+        __syncwarp();
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar_teardown, 0) && ptx::globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int row = threadIdx.x;                    // TMEM lane
+    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+    const bool row_valid = row < p.R;
+    const int s_q = row_valid ? row / p.G : 0;      // query position of this row
+    const int hq = kvh * p.G + (row_valid ? row % p.G : 0);
+    const float sl2 = p.scale_log2;
+    int lim_abs = p.Sk;                             // exclusive key bound of this row
+    if (p.causal) {
+      const long long l2 = static_cast<long long>(s_q) + p.Sk - p.Sq + 1;
+      lim_abs = static_cast<int>(l2 < 0 ? 0 : (l2 > p.Sk ? p.Sk : l2));
+    }
+    float m_ref = kNegInf, l_exact = 0.0f, l_corr = 0.0f;
+    bool ok = true;
+    for (int j = 0; ok && j < n; ++j) {
+      const uint32_t tS = tmem + lane_bits + 128 * (j & 1);
+      if (!(ok = dec_wait(bar_s_full + 8 * (j & 1), (j >> 1) & 1, abort_flag, p))) break;
+      ptx::tc_fence_after();
+      uint32_t sr[128];
+      ptx::tmem_ld_32x32b_x128(tS, sr);
+      float s[128];
+      const int lim = lim_abs - (t_begin + j) * 128;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? __uint_as_float(sr[c]) : kNegInf;
+      float mq[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mq[c] = s[c];
+#pragma unroll
+      for (int c = 8; c < 128; c += 16) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mq[q] = ptx::max3(mq[q], s[c + 2 * q], s[c + 2 * q + 1]);
+      }
+      const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
+      const float m_new = fmaxf(m_ref, mx * sl2);
+      float alpha = 1.0f;
+      const bool need = m_new > m_ref + kRescale;
+      if (need) {
+        alpha = ptx::ex2_approx(m_ref - m_new);
+        m_ref = m_new;
+        l_exact *= alpha;
+        l_corr *= alpha;
+      }
+      const float neg_m = (m_ref == kNegInf) ? 0.0f : -m_ref;
+      {
+        const float pmax = ptx::ex2_approx(fmaf(mx, sl2, neg_m));
+        const uint32_t pr = dec_pack2<BF16>(pmax, 0.0f);
+        float pmax_r, unused;
+        if constexpr (BF16) pmax_r = __uint_as_float(pr << 16);
+        else ptx::f16x2_to_f32(pr, pmax_r, unused);
+        l_corr += pmax_r - pmax;
+      }
+      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2), negm2 = ptx::f2_pack(neg_m, neg_m);
+      uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int e = 64 * h + 2 * c;
+          float t0, t1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[e], s[e + 1]), sl2x2, negm2), t0, t1);
+          const float p0 = ptx::ex2_approx(t0), p1 = ptx::ex2_approx(t1);
+          pk[c] = dec_pack2<BF16>(p0, p1);
+          if (c & 1) acc1 = ptx::f2_add(acc1, ptx::f2_pack(p0, p1));
+          else acc0 = ptx::f2_add(acc0, ptx::f2_pack(p0, p1));
+        }
+        ptx::tmem_st_32x32b_x32(tS + 32 * h, pk);
+      }
+      {
+        float a0, a1;
+        ptx::f2_unpack(ptx::f2_add(acc0, acc1), a0, a1);
+        l_exact += a0 + a1;
+      }
+      // P V of the previous key tile must have completed before O~ is rescaled
+      if (j > 0) {
+        if (!(ok = dec_wait(bar_pv_done, (j - 1) & 1, abort_flag, p))) break;
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          const uint64_t a2 = ptx::f2_pack(alpha, alpha);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_bits + 256 + c * 32, orr);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2),
+                             x0, x1);
+              orr[e] = __float_as_uint(x0);
+              orr[e + 1] = __float_as_uint(x1);
+            }
+            ptx::tmem_st_32x32b_x32(tmem + lane_bits + 256 + c * 32, orr);
+          }
+        }
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_p_full);
+    }
+    // ---- epilogue
+    uint32_t orr[D];
+    bool have_o = false;
+    if (ok && n > 0) {
+      if ((ok = dec_wait(bar_o_full, 0, abort_flag, p))) {
+        ptx::tc_fence_after();
+        if constexpr (D == 128) ptx::tmem_ld_32x32b_x128(tmem + lane_bits + 256, orr);
+        else ptx::tmem_ld_32x32b_x64(tmem + lane_bits + 256, orr);
+        have_o = true;
+      }
+    }
+    const bool live = have_o && l_exact > 0.0f;
+    const float inv_l = live ? __frcp_rn(l_exact + l_corr) : 0.0f;
+    const float lse = live ? (m_ref + __log2f(l_exact)) * 0.69314718055994531f : kNegInf;
+    if (row_valid && (ok || n == 0)) {
+      const long long orow = (static_cast<long long>(b) * p.Sq + s_q) * p.Hq + hq;
+      const long long lidx = (static_cast<long long>(b) * p.Hq + hq) * p.Sq + s_q;
+      if (p.n_splits == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          float x[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] = live ? __uint_as_float(orr[8 * c + q]) * inv_l : 0.0f;
+          dst[c] = make_uint4(dec_pack2<BF16>(x[0], x[1]), dec_pack2<BF16>(x[2], x[3]), dec_pack2<BF16>(x[4], x[5]),
+                              dec_pack2<BF16>(x[6], x[7]));
+        }
+        if (p.lse) p.lse[lidx] = lse;
+      } else {
+        const long long rows_all = static_cast<long long>(p.B) * p.Sq * p.Hq;
+        float4* dst = reinterpret_cast<float4*>(p.o_part + (split * rows_all + orow) * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) {
+          float4 v;
+          v.x = live ? __uint_as_float(orr[4 * c + 0]) * inv_l : 0.0f;
+          v.y = live ? __uint_as_float(orr[4 * c + 1]) * inv_l : 0.0f;
+          v.z = live ? __uint_as_float(orr[4 * c + 2]) * inv_l : 0.0f;
+          v.w = live ? __uint_as_float(orr[4 * c + 3]) * inv_l : 0.0f;
+          dst[c] = v;
+        }
+        p.lse_part[split * rows_all + lidx] = lse;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 5) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace fa

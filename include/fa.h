@@ -112,6 +112,36 @@ int fa_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o, 
              int D, int dtype, fa_stream_t stream);
 
 /*
+ * fa_fwd_decode — attention for few query rows per KV head (decode, short
+ * chunks), split over the keys. The Hq/Hkv query heads of a KV group and the
+ * Sq query positions form the rows of one tile, so (Hq/Hkv) * Sq <= 128 is
+ * required (else FA_ERR_UNSUPPORTED: use fa_fwd). The keys are cut into
+ * `num_splits` ranges of whole 128-key tiles (num_splits <= 0 picks about
+ * two waves of CTAs on the current device; the count is clamped to the
+ * number of key tiles), each range gives a normalised partial (O_s, LSE_s),
+ * and fa_merge's rule combines them into O and LSE. Layouts, dtypes, mask
+ * and errors as for fa_fwd (contiguous tensors).
+ * workspace        device scratch of at least the size returned by
+ *                  fa_decode_workspace_size for the same arguments and
+ *                  current device, 16-byte aligned, owned by the caller and
+ *                  used only until the call's work on `stream` completes; it
+ *                  may be NULL when that size is 0 (one split). A smaller or
+ *                  NULL workspace when one is needed gives FA_ERR_INVALID_ARG.
+ * Two calls that share a workspace must not overlap on the device.
+ */
+int fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk, int Hq,
+                  int Hkv, int D, float scale, int causal, int dtype, int num_splits, void* workspace,
+                  unsigned long long workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_decode_workspace_size — bytes of workspace fa_fwd_decode needs for
+ * these sizes and `num_splits` (written to *bytes; 0 when one split
+ * suffices). Errors as for fa_fwd_decode's size checks.
+ */
+int fa_decode_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D, int num_splits,
+                             unsigned long long* bytes);
+
+/*
  * fa_status — synchronise `stream`, then read and clear the device status
  * word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's bounded
  * wait on an mbarrier ran out (the kernel then released its tensor memory

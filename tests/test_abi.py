@@ -131,3 +131,38 @@ def test_strided_entry_rejects_null_strides(lib):
 ])
 def test_merge_validates_before_any_launch(lib, args, code):
     assert lib.fa_merge(*args, None) == code
+
+
+def test_decode_workspace_size_formula(lib):
+    out = ctypes.c_ulonglong(7)
+    # explicit 4 splits of 2048 keys (16 tiles): 4 x rows x (D + 1) floats, LSE part padded to 16 bytes
+    assert lib.fa_decode_workspace_size(2, 1, 2048, 32, 4, 128, 4, ctypes.byref(out)) == api.FA_OK
+    rows = 2 * 1 * 32
+    assert out.value == 4 * rows * 128 * 4 + (4 * rows * 4 + 15) // 16 * 16
+    # one split: no workspace
+    assert lib.fa_decode_workspace_size(2, 1, 2048, 32, 4, 128, 1, ctypes.byref(out)) == api.FA_OK
+    assert out.value == 0
+    # more splits than key tiles are clamped to the tile count (2 tiles)
+    assert lib.fa_decode_workspace_size(1, 1, 200, 8, 8, 64, 9, ctypes.byref(out)) == api.FA_OK
+    assert out.value == 2 * 8 * 64 * 4 + (2 * 8 * 4 + 15) // 16 * 16
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 17, 100, 64, 8, 128, 0), api.FA_ERR_UNSUPPORTED),    # 8 heads x 17 positions > 128 rows
+    ((1, 1, 100, 6, 4, 128, 0), api.FA_ERR_INVALID_ARG),      # Hq not a multiple of Hkv
+    ((1, 1, 100, 8, 8, 96, 0), api.FA_ERR_UNSUPPORTED),       # D
+])
+def test_decode_size_checks(lib, args, code):
+    out = ctypes.c_ulonglong(0)
+    assert lib.fa_decode_workspace_size(*args, ctypes.byref(out)) == code
+
+
+def test_decode_rejects_before_any_launch(lib):
+    c = lambda **kw: lib.fa_fwd_decode(16, 16, 16, 16, None, kw.get("B", 1), kw.get("Sq", 1), 64, kw.get("Hq", 8),
+                                       kw.get("Hkv", 2), 128, ctypes.c_float(kw.get("scale", 0.1)),
+                                       kw.get("causal", 0), kw.get("dtype", 1), 0, None, 0, None)
+    assert c(dtype=5) == api.FA_ERR_INVALID_ARG
+    assert c(causal=3) == api.FA_ERR_INVALID_ARG
+    assert c(scale=0.0) == api.FA_ERR_INVALID_ARG
+    assert c(Sq=40) == api.FA_ERR_UNSUPPORTED
+    assert c(B=0) == api.FA_OK

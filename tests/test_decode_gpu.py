@@ -1,0 +1,70 @@
+"""fa_fwd_decode (split-KV over the keys, per-split partials merged) against
+the fp64 oracle, every element, over decode-like shapes: one or a few query
+positions, GQA groups packed into one tile, causal and not, ragged key
+counts, one split, automatic splits and explicit split counts."""
+
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from exact_attention_16_gb300 import api  # noqa: E402
+from exact_attention_16_gb300.workloads import Workload, draw_inputs  # noqa: E402
+
+from parity import compare  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def W(B, Sq, Sk, Hq, Hkv, D, dtype="bf16", causal=True, sigma=1.0, seed=31):
+    return Workload("dec", B, Sq, Sk, Hq, Hkv, D, dtype, causal, sigma, 1.0, seed)
+
+
+CASES = [
+    (W(2, 1, 3000, 32, 4, 128), 0),              # GQA 8, one query, automatic splits
+    (W(2, 1, 3000, 32, 4, 128, causal=False), 5),
+    (W(1, 4, 1037, 16, 2, 128), 0),              # 8 heads x 4 positions = 32 rows
+    (W(1, 16, 700, 64, 8, 128), 3),              # 8 x 16 = 128 rows (a full tile)
+    (W(3, 1, 513, 8, 8, 64, "fp16"), 0),         # MHA decode, D = 64
+    (W(1, 2, 100, 4, 1, 128), 0),                # fewer keys than one tile
+    (W(1, 8, 5, 4, 2, 128), 1),                  # Sq > Sk, causal: first rows see nothing
+    (W(2, 1, 4096, 16, 8, 128, sigma=2.0), 1),   # one split writes O directly
+    (W(1, 1, 2048, 32, 4, 128), 16),             # as many splits as key tiles
+]
+
+
+@pytest.mark.parametrize("w,splits", CASES, ids=lambda x: str(x) if isinstance(x, int) else
+                         f"B{x.B}_Sq{x.Sq}_Sk{x.Sk}_H{x.Hq}-{x.Hkv}_D{x.D}_{x.dtype}_{'c' if x.causal else 'n'}")
+def test_decode_every_element(w, splits):
+    import oracle
+    q, k, v = draw_inputs(w)
+    o, lse = api.fa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), scale=w.scale, causal=w.causal, num_splits=splits)
+    assert api.fa_status() == 0
+    o_ref, l_ref = oracle.attention(q.float().numpy(), k.float().numpy(), v.float().numpy(), w.scale, w.causal)
+    compare(o.float().cpu().numpy().transpose(0, 2, 1, 3), lse.cpu().numpy(), o_ref.transpose(0, 2, 1, 3), l_ref)
+
+
+def test_decode_matches_prefill_kernel():
+    """Same inputs through fa_fwd and fa_fwd_decode: both within tolerance of
+    each other (different key grouping, same arithmetic)."""
+    w = W(2, 2, 2500, 32, 4, 128)
+    q, k, v = (t.cuda() for t in draw_inputs(w))
+    o1, l1 = api.fa_fwd(q, k, v, causal=True)
+    o2, l2 = api.fa_fwd_decode(q, k, v, causal=True)
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+def test_decode_rejects_small_workspace():
+    w = W(1, 1, 2048, 32, 4, 128)
+    q, k, v = (t.cuda() for t in draw_inputs(w))
+    need = api.fa_decode_workspace_size(1, 1, 2048, 32, 4, 128, 4)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(api.FAError):
+        api.fa_fwd_decode(q, k, v, causal=True, num_splits=4, workspace=small)
