@@ -353,6 +353,68 @@ def run_merge(args, w):
     }
 
 
+def run_decode(args, w):
+    """Split-KV decode: one query position per sequence against the
+    workload's keys, batch `args.decode_batch`. HBM-bound (every K/V byte is
+    read once per step), reported in GB/s of algorithmic bytes."""
+    import torch
+
+    from exact_attention_16_gb300 import api
+    from exact_attention_16_gb300.workloads import Workload
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wd = Workload(f"decode_{w.name}", args.decode_batch, 1, w.Sk, w.Hq, w.Hkv, w.D, w.dtype, True, w.sigma_qk,
+                  w.sigma_v, w.seed)
+    q, k, v = (t.to(dev) for t in draw_inputs(wd))
+    out = torch.empty_like(q)
+    lse = torch.empty((wd.B, wd.Hq, 1), dtype=torch.float32, device=dev)
+    need = api.fa_decode_workspace_size(wd.B, 1, wd.Sk, wd.Hq, wd.Hkv, wd.D, 0)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    nbytes = metrics.algorithmic_bytes(wd.B, 1, wd.Sk, wd.Hq, wd.Hkv, wd.D)
+
+    def step():
+        api.fa_fwd_decode(q, k, v, scale=wd.scale, causal=True, workspace=ws, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if api.fa_status() != 0:
+        raise RuntimeError("device status not OK")
+    launch_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    peaks = measured_peaks()
+    avg = sum(launch_ms) / len(launch_ms)
+    value = nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    return rank, {
+        "metric": "decode attention GB/s (algorithmic bytes: Q, K, V read once, O and LSE written once)",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wd.dtype, "data": "synthetic (seeded PCG64 normal draws rounded to the dtype)",
+        "config": {"workload": wd.name, "B": wd.B, "Sq": 1, "Sk": wd.Sk, "Hq": wd.Hq, "Hkv": wd.Hkv, "D": wd.D,
+                   "bytes_per_step": nbytes, "workspace_bytes": need,
+                   "l2": f"K+V {nbytes >> 20} MiB" + (" > 129 MB L2; no flush" if nbytes > L2_BYTES else
+                                                       " (smaller than L2: hot-L2 figure)")},
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / (avg * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(nbytes / (avg * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"] + " copy bandwidth", "traffic": None,
+                     "kernel": "fa_decode_kernel + merge_kernel", "avg_launch_ms": round(avg, 4)},
+        "gpu_launches": 2 * args.steps if need > 0 else args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def oracle_sample(w, q32, k32, v32, rows_per_head: int, n_heads: int):
     """Time the oracle on the last `rows_per_head` rows of the first heads;
     returns (seconds, flops done)."""
@@ -443,8 +505,9 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["fwd", "merge"], default="fwd",
-                    help="fwd: the attention forward (default); merge: partial-state merge")
+    ap.add_argument("--op", choices=["fwd", "merge", "decode"], default="fwd",
+                    help="fwd: the attention forward (default); merge: partial-state merge; decode: split-KV decode")
+    ap.add_argument("--decode-batch", type=int, default=16, help="sequences per step for --op decode")
     ap.add_argument("--parts", type=int, default=4, help="partial states for --op merge")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[x.name for x in WORKLOADS])
     ap.add_argument("--cpu-budget", type=float, default=18.0, help="seconds of oracle work for cpu_baseline")
@@ -457,6 +520,8 @@ def main():
         rank, res = run_reference(args, w)
     elif args.op == "merge":
         rank, res = run_merge(args, w)
+    elif args.op == "decode":
+        rank, res = run_decode(args, w)
     else:
         rank, res = run_ours(args, w)
     if rank == 0 and res is not None:
