@@ -23,6 +23,7 @@ __all__ = [
     "fa_merge",
     "fa_fwd_decode",
     "fa_decode_workspace_size",
+    "fa_fwd_decode_noalloc",
     "fa_status",
     "fa_status_string",
     "fa_version",
@@ -59,6 +60,10 @@ EXPORTED_SYMBOLS = {
     "fa_decode_workspace_size": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_fwd_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_void_p]),
     "fa_status": (ctypes.c_int, [ctypes.c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_version": (ctypes.c_int, []),
@@ -249,6 +254,36 @@ def fa_fwd_decode(q, k, v, *, scale=None, causal=False, num_splits=0, workspace=
                                  _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_decode")
+    return out, lse
+
+
+def fa_fwd_decode_noalloc(q, k, v, *, scale=None, causal=False, num_splits=0, out=None, lse=None,
+                          return_lse=True, stream=None):
+    """fa_fwd_decode whose split workspace is the library's fixed 16 MiB
+    device array, for callers that cannot allocate device memory when they
+    call (see include/fa.h). Calls that overlap on the GPU share that array
+    and race; order them on one stream."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         lse.data_ptr() if lse is not None else None, B, Sq, Sk, Hq, Hkv, D,
+                                         float(scale), int(bool(causal)), code, int(num_splits),
+                                         _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_decode_noalloc")
     return out, lse
 
 

@@ -1,0 +1,61 @@
+// fa_fwd_decode_noalloc: the split-KV decode call for callers that cannot
+// allocate device memory at call time. Such callers include code running
+// under a memory manager that owns the whole device heap (for example a
+// serving process whose memory plan is fixed when it starts), and code that
+// must not allocate on its hot path because an allocation can block on the
+// device or fail once memory is fragmented. The split workspace of
+// fa_fwd_decode lives here in a fixed-size array in the library's own
+// device memory instead of in a caller-provided buffer.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+
+namespace {
+
+// Scratch for the per-split partial states (fp32 O and LSE). Every device
+// that loads this library holds these bytes until the process exits.
+constexpr unsigned long long kScratchBytes = 16ull << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_once[kMaxDevices];
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+cudaError_t g_scratch_err[kMaxDevices] = {cudaSuccess};
+
+// Device address of g_decode_scratch on the current device. In host code the
+// array's name only stands for the symbol; the address a kernel may use has
+// to come from the runtime, once per device, with that device current.
+void* scratch_address(int dev) {
+  std::call_once(g_once[dev], [dev] {
+    void* ptr = nullptr;
+    g_scratch_err[dev] = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    g_scratch_addr[dev] = g_scratch_err[dev] == cudaSuccess ? ptr : nullptr;
+  });
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq,
+                                     int Sk, int Hq, int Hkv, int D, float scale, int causal, int dtype,
+                                     int num_splits, fa_stream_t stream) {
+  // Same sizes and checks as fa_fwd_decode; the workspace the call needs must
+  // fit the fixed scratch array.
+  unsigned long long need = 0;
+  int rc = fa_decode_workspace_size(B, Sq, Sk, Hq, Hkv, D, num_splits, &need);
+  if (rc != FA_OK) return rc;
+  if (need > kScratchBytes) return FA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (need > 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    scratch = scratch_address(dev);
+    if (!scratch) return FA_ERR_CUDA;
+  }
+  // Every split writes all of its partial rows before the merge reads them,
+  // so nothing in the scratch has to start at zero.
+  return fa_fwd_decode(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, dtype, num_splits, scratch,
+                       need > 0 ? kScratchBytes : 0, stream);
+}

@@ -142,6 +142,30 @@ int fa_decode_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D, int 
                              unsigned long long* bytes);
 
 /*
+ * fa_fwd_decode_noalloc — fa_fwd_decode without a caller-provided workspace,
+ * for callers that cannot allocate device memory when they call: code under
+ * a memory manager that owns the whole device heap (for example a serving
+ * process whose memory plan is fixed at start-up), or code that must not
+ * allocate on its hot path because an allocation can block on the device or
+ * fail once memory is fragmented. No page describes this call; it exists
+ * for those callers only.
+ * The split workspace is a fixed 16 MiB array in the library's own device
+ * memory, which every GPU that loads the library holds until the process
+ * exits. A call whose workspace (fa_decode_workspace_size for the same
+ * arguments) exceeds 16 MiB returns FA_ERR_UNSUPPORTED; a smaller num_splits
+ * or fa_fwd_decode with a workspace serves those sizes. The call allocates
+ * nothing (no cudaMalloc/cudaFree). The first call on a device looks up the
+ * array's device address on that device (once per device, with the device
+ * current); make that first call before any stream capture. Every call on a
+ * device shares the one array, so calls that overlap on the GPU (different
+ * streams, or host threads without ordering) race on it; order them on one
+ * stream. Arguments, results and errors are otherwise those of fa_fwd_decode.
+ */
+int fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
+                          int Hq, int Hkv, int D, float scale, int causal, int dtype, int num_splits,
+                          fa_stream_t stream);
+
+/*
  * fa_status — synchronise `stream`, then read and clear the device status
  * word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's bounded
  * wait on an mbarrier ran out (the kernel then released its tensor memory
