@@ -415,6 +415,64 @@ def run_decode(args, w):
     }
 
 
+def run_splitkv(args, w):
+    """The workload as given through the split-KV path (fa_fwd_decode), which
+    serves small prefill problems that leave fa_fwd's persistent grid
+    partly idle; same TFLOP/s metric as the default leg."""
+    import torch
+
+    from exact_attention_16_gb300 import api
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = (t.to(dev) for t in draw_inputs(w))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    need = api.fa_decode_workspace_size(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D, 0)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    flop = metrics.flops(w.B, w.Sq, w.Sk, w.Hq, w.D, w.causal)
+    in_bytes = sum(x.numel() * x.element_size() for x in (q, k, v))
+    flush = None if in_bytes > L2_BYTES else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        api.fa_fwd_decode(q, k, v, scale=w.scale, causal=w.causal, workspace=ws, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if api.fa_status() != 0:
+        raise RuntimeError("device status not OK")
+    launch_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    total_ms = starts[0].elapsed_time(ends[-1]) if flush is None else sum(launch_ms)
+    peaks = measured_peaks()
+    value = whole_job_tflops(1, flop, args.steps, total_ms)
+    return rank, {
+        "metric": METRIC + " (split-KV path)", "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded PCG64 normal draws rounded to the dtype)",
+        "config": {"workload": w.name, "path": "fa_fwd_decode", "workspace_bytes": need,
+                   "l2": "no flush (inputs > L2)" if flush is None else
+                         "256 MiB L2 flush before each launch, excluded from the event timing"},
+        "pct_of_peak": round(100.0 * value / peaks["bf16_tflops"], 2),
+        "gpu_launches": (2 if need > 0 else 1) * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def oracle_sample(w, q32, k32, v32, rows_per_head: int, n_heads: int):
     """Time the oracle on the last `rows_per_head` rows of the first heads;
     returns (seconds, flops done)."""
@@ -505,8 +563,9 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["fwd", "merge", "decode"], default="fwd",
-                    help="fwd: the attention forward (default); merge: partial-state merge; decode: split-KV decode")
+    ap.add_argument("--op", choices=["fwd", "merge", "decode", "splitkv"], default="fwd",
+                    help="fwd: the attention forward (default); merge: partial-state merge; decode: split-KV "
+                         "decode; splitkv: the workload through the split-KV path")
     ap.add_argument("--decode-batch", type=int, default=16, help="sequences per step for --op decode")
     ap.add_argument("--parts", type=int, default=4, help="partial states for --op merge")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[x.name for x in WORKLOADS])
@@ -522,6 +581,8 @@ def main():
         rank, res = run_merge(args, w)
     elif args.op == "decode":
         rank, res = run_decode(args, w)
+    elif args.op == "splitkv":
+        rank, res = run_splitkv(args, w)
     else:
         rank, res = run_ours(args, w)
     if rank == 0 and res is not None:

@@ -22,7 +22,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct Plan {
-  int n_tiles = 0, n_splits = 1, tiles_per_split = 0;
+  int n_tiles = 0, n_splits = 1, positions = 1, n_row_tiles = 1;
   unsigned long long o_part_bytes = 0, lse_part_bytes = 0;
   unsigned long long workspace_bytes() const { return n_splits > 1 ? o_part_bytes + lse_part_bytes : 0; }
 };
@@ -35,21 +35,24 @@ int device_sms() {
   return sms[dev];
 }
 
-// Splits of the key range: the requested number, or (num_splits <= 0) enough
-// to give about two waves of CTAs on `sms` SMs; every split has >= 1 tile.
+// Row tiles of floor(128 / G) query positions, and splits of the key range:
+// the requested number, or (num_splits <= 0) enough to give about two waves
+// of CTAs on `sms` SMs; at most one split per key tile.
 Plan make_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int num_splits, int sms) {
   Plan pl;
   pl.n_tiles = (Sk + 127) / 128;
+  const int G = Hkv > 0 ? Hq / Hkv : 1;
+  pl.positions = G > 0 ? 128 / G : 1;
+  pl.n_row_tiles = (Sq + pl.positions - 1) / pl.positions;
   int want = num_splits;
   if (want <= 0) {
-    const long long units = static_cast<long long>(B) * Hkv;
+    const long long units = static_cast<long long>(B) * Hkv * pl.n_row_tiles;
     const long long target = 2LL * (sms > 0 ? sms : 148);
     want = static_cast<int>(units >= target ? 1 : (target + units - 1) / units);
   }
   if (want > pl.n_tiles) want = pl.n_tiles;
   if (want < 1) want = 1;
-  pl.tiles_per_split = pl.n_tiles > 0 ? (pl.n_tiles + want - 1) / want : 0;
-  pl.n_splits = pl.tiles_per_split > 0 ? (pl.n_tiles + pl.tiles_per_split - 1) / pl.tiles_per_split : 1;
+  pl.n_splits = want;
   const unsigned long long rows = static_cast<unsigned long long>(B) * Sq * Hq;
   pl.o_part_bytes = static_cast<unsigned long long>(pl.n_splits) * rows * D * 4;
   pl.lse_part_bytes = (static_cast<unsigned long long>(pl.n_splits) * rows * 4 + 15) / 16 * 16;
@@ -63,7 +66,7 @@ int check_args(int B, int Sq, int Sk, int Hq, int Hkv, int D, int dtype) {
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(Hq / Hkv) * Sq > 128) return FA_ERR_UNSUPPORTED;   // rows per KV head in one tile
+  if (Hq / Hkv > 128) return FA_ERR_UNSUPPORTED;   // one query position of a whole group must fit a tile
   return FA_OK;
 }
 
@@ -109,7 +112,7 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   const long long skv[3] = {static_cast<long long>(Sk) * Hkv * D, static_cast<long long>(Hkv) * D, D};
   const int G = Hq / Hkv;
   CUtensorMap tq, tk, tv;
-  if (!encode_bshd_box(&tq, q, bf16, B, Sq, Hq, D, sq, G, Sq) ||
+  if (!encode_bshd_box(&tq, q, bf16, B, Sq, Hq, D, sq, G, pl.positions) ||
       !encode_bshd_box(&tk, k, bf16, B, Sk, Hkv, D, skv, 1, 128) ||
       !encode_bshd_box(&tv, v, bf16, B, Sk, Hkv, D, skv, 1, 128))
     return FA_ERR_CUDA;
@@ -118,15 +121,18 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   p.lse = lse;
   p.o_part = o_part;
   p.lse_part = lse_part;
-  p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.R = G * Sq;
+  p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.G = G;
+  p.P = pl.positions;
+  p.n_row_tiles = pl.n_row_tiles;
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.n_splits = pl.n_splits;
-  p.tiles_per_split = pl.tiles_per_split;
   p.n_kv_tiles = pl.n_tiles;
   p.timeout_ns = timeout_ns();
   p.status = status_word;
-  const dim3 grid(pl.n_splits, Hkv, B);
+  const long long gx = static_cast<long long>(pl.n_splits) * pl.n_row_tiles;
+  if (gx > 0x7fffffffLL || Hkv > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(gx), Hkv, B);
   int rc = D == 128 ? (bf16 ? launch_decode<128, true>(tq, tk, tv, p, grid, stream)
                             : launch_decode<128, false>(tq, tk, tv, p, grid, stream))
                     : (bf16 ? launch_decode<64, true>(tq, tk, tv, p, grid, stream)

@@ -1,16 +1,18 @@
-// Split-KV attention for few query rows per KV head (decode and short
-// chunks), sm_103a. One CTA handles the G x Sq query rows that share one KV
-// head (GQA group x query positions, "MiniPaged-Qwen: Qwen3 Prefill
-// FlashAttention" section 6) against one contiguous range of 128-key tiles
-// (a split); the per-split results are normalised partial states (O_s,
-// LSE_s) that a merge combines, or the final O when there is one split.
+// Split-KV attention, sm_103a: decode, short chunks and small prefill. One
+// CTA handles one row tile of the query rows that share a KV head (the G
+// heads of a GQA group times P = floor(128 / G) query positions, "MiniPaged-
+// Qwen: Qwen3 Prefill FlashAttention" section 6) against one contiguous
+// range of 128-key tiles (a split); the per-split results are normalised
+// partial states (O_s, LSE_s) that a merge combines, or the final O when
+// there is one split.
 // Same arithmetic as the prefill kernel (online softmax with exp2 and the
 // log2e-folded scale, bottom-right causal limit of section 13): TMA K/V
 // ring, tcgen05 Q K^T into a double-buffered S in tensor memory, softmax by
 // one thread per row, P V with P read from tensor memory.
 //
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (TMEM lanes 0-127,
-// row r = s * G + g), warp 4 TMA producer, warp 5 MMA issuer / TMEM owner.
+// row r = s_local * G + g), warp 4 TMA producer, warp 5 MMA issuer / TMEM
+// owner. Grid: x = split + n_splits * row tile, y = KV head, z = batch.
 // TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256, 256+D).
 #pragma once
 
@@ -26,10 +28,12 @@ struct DecodeParams {
   float* lse;          // final LSE (B, Hq, Sq) or null (one split)
   float* o_part;       // (n_splits, B, Sq, Hq, D) fp32 partial O (several splits)
   float* lse_part;     // (n_splits, B, Hq, Sq) fp32 partial LSE
-  int B, Sq, Sk, Hq, Hkv, G, R;    // R = G * Sq query rows per CTA (<= 128)
+  int B, Sq, Sk, Hq, Hkv, G;
+  int P;               // query positions per row tile: floor(128 / G)
+  int n_row_tiles;     // ceil(Sq / P)
   int causal;
   float scale_log2;
-  int n_splits, tiles_per_split, n_kv_tiles;
+  int n_splits, n_kv_tiles;
   unsigned long long timeout_ns;
   int* status;
 };
@@ -100,16 +104,27 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int t_begin = split * p.tiles_per_split;
-  const int t_end = min(p.n_kv_tiles, t_begin + p.tiles_per_split);
-  const int n = max(0, t_end - t_begin);
+  const int split = blockIdx.x % p.n_splits, rt = blockIdx.x / p.n_splits;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int pos0 = rt * p.P;                                  // first query position of the tile
+  const int rows_box = p.G * p.P;                              // rows the Q box fills
+  // key tiles this row tile needs (bottom-right causal limit of its last row)
+  int n_need = p.n_kv_tiles;
+  if (p.causal) {
+    const long long last = static_cast<long long>(min(pos0 + p.P, p.Sq)) - 1;
+    long long lim = last + p.Sk - p.Sq + 1;
+    if (lim > p.Sk) lim = p.Sk;
+    n_need = lim <= 0 ? 0 : static_cast<int>((lim + 127) / 128);
+  }
+  const int tps = (n_need + p.n_splits - 1) / p.n_splits;
+  const int t_begin = split * tps;
+  const int n = max(0, min(n_need, t_begin + tps) - t_begin);
 
-  // Rows R..127 of the Q tile are never loaded: zero them so that the
+  // Rows past G * P of the Q tile are never loaded: zero them so that the
   // unused rows of S, P and O stay finite.
   for (int i = threadIdx.x; i < L::kTileBytes / 16; i += blockDim.x) {
     const int row = (i * 16 / 128) % 128;
-    if (row >= p.R) reinterpret_cast<uint4*>(base_ptr + L::kQOff)[i] = make_uint4(0, 0, 0, 0);
+    if (row >= rows_box) reinterpret_cast<uint4*>(base_ptr + L::kQOff)[i] = make_uint4(0, 0, 0, 0);
   }
   ptx::fence_proxy_async_smem();
   if (threadIdx.x == 0) {
@@ -142,11 +157,11 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint32_t issued = 0;
     if (n > 0 && lane == 0) {
       const uint64_t pol_kv = ptx::policy_evict_first();   // each K/V byte is read once
-      const uint32_t q_bytes = static_cast<uint32_t>(p.R) * 128u * L::kChunks;
+      const uint32_t q_bytes = static_cast<uint32_t>(rows_box) * 128u * L::kChunks;
       ptx::mbar_arrive_expect_tx(bar_q_full, q_bytes);
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
-        ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, 0, b, pol_kv);
+        ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, pos0, b, pol_kv);
       for (int j = 0; ok && j < 2 * n; ++j) {               // K_0, V_0, K_1, V_1, ...
         const uint32_t st = j % kStages, ph = ((j / kStages) & 1u) ^ 1u;
         if (!(ok = dec_wait(bar_kv_empty + 8 * st, ph, abort_flag, p))) break;
@@ -235,8 +250,8 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ------------------------------------------------------------ softmax + epilogue
     const int row = threadIdx.x;                    // TMEM lane
     const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-    const bool row_valid = row < p.R;
-    const int s_q = row_valid ? row / p.G : 0;      // query position of this row
+    const bool row_valid = row < rows_box && pos0 + row / p.G < p.Sq;
+    const int s_q = row_valid ? pos0 + row / p.G : 0;   // query position of this row
     const int hq = kvh * p.G + (row_valid ? row % p.G : 0);
     const float sl2 = p.scale_log2;
     int lim_abs = p.Sk;                             // exclusive key bound of this row

@@ -112,15 +112,16 @@ int fa_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o, 
              int D, int dtype, fa_stream_t stream);
 
 /*
- * fa_fwd_decode — attention for few query rows per KV head (decode, short
- * chunks), split over the keys. The Hq/Hkv query heads of a KV group and the
- * Sq query positions form the rows of one tile, so (Hq/Hkv) * Sq <= 128 is
- * required (else FA_ERR_UNSUPPORTED: use fa_fwd). The keys are cut into
- * `num_splits` ranges of whole 128-key tiles (num_splits <= 0 picks about
- * two waves of CTAs on the current device; the count is clamped to the
- * number of key tiles), each range gives a normalised partial (O_s, LSE_s),
- * and fa_merge's rule combines them into O and LSE. Layouts, dtypes, mask
- * and errors as for fa_fwd (contiguous tensors).
+ * fa_fwd_decode — attention split over the keys: decode, short chunks and
+ * small prefill problems (too few (batch, head, row tile) units to fill the
+ * GPU with fa_fwd). The Hq/Hkv query heads of a KV group times
+ * floor(128 / (Hq/Hkv)) query positions form one row tile, so Hq/Hkv <= 128
+ * is required (else FA_ERR_UNSUPPORTED). The keys are cut into `num_splits`
+ * ranges of whole 128-key tiles (num_splits <= 0 picks about two waves of
+ * CTAs on the current device; the count is clamped to the number of key
+ * tiles), each range gives a normalised partial (O_s, LSE_s), and fa_merge's
+ * rule combines them into O and LSE. Layouts, dtypes, mask and errors as for
+ * fa_fwd (contiguous tensors).
  * workspace        device scratch of at least the size returned by
  *                  fa_decode_workspace_size for the same arguments and
  *                  current device, 16-byte aligned, owned by the caller and

@@ -148,7 +148,7 @@ def test_decode_workspace_size_formula(lib):
 
 
 @pytest.mark.parametrize("args,code", [
-    ((1, 17, 100, 64, 8, 128, 0), api.FA_ERR_UNSUPPORTED),    # 8 heads x 17 positions > 128 rows
+    ((1, 17, 100, 256, 1, 128, 0), api.FA_ERR_UNSUPPORTED),   # 256 query heads per KV head > 128 rows
     ((1, 1, 100, 6, 4, 128, 0), api.FA_ERR_INVALID_ARG),      # Hq not a multiple of Hkv
     ((1, 1, 100, 8, 8, 96, 0), api.FA_ERR_UNSUPPORTED),       # D
 ])
@@ -164,5 +164,5 @@ def test_decode_rejects_before_any_launch(lib):
     assert c(dtype=5) == api.FA_ERR_INVALID_ARG
     assert c(causal=3) == api.FA_ERR_INVALID_ARG
     assert c(scale=0.0) == api.FA_ERR_INVALID_ARG
-    assert c(Sq=40) == api.FA_ERR_UNSUPPORTED
+    assert c(Hq=258, Hkv=2) == api.FA_ERR_UNSUPPORTED
     assert c(B=0) == api.FA_OK

@@ -1,7 +1,8 @@
 """fa_fwd_decode (split-KV over the keys, per-split partials merged) against
-the fp64 oracle, every element, over decode-like shapes: one or a few query
-positions, GQA groups packed into one tile, causal and not, ragged key
-counts, one split, automatic splits and explicit split counts."""
+the fp64 oracle, every element, over decode-like shapes (one or a few query
+positions, GQA groups packed into one tile) and small prefill shapes (several
+row tiles of floor(128 / G) positions), causal and not, ragged key counts,
+one split, automatic splits and explicit split counts."""
 
 import pytest
 
@@ -35,6 +36,11 @@ CASES = [
     (W(1, 8, 5, 4, 2, 128), 1),                  # Sq > Sk, causal: first rows see nothing
     (W(2, 1, 4096, 16, 8, 128, sigma=2.0), 1),   # one split writes O directly
     (W(1, 1, 2048, 32, 4, 128), 16),             # as many splits as key tiles
+    # prefill-sized query counts: several row tiles of floor(128 / G) positions
+    (W(1, 1280, 1536, 16, 16, 128, "fp16"), 0),  # MHA, 128 positions per tile, offset 256
+    (W(2, 300, 333, 8, 2, 128), 3),              # G = 4: 32 positions per tile, ragged
+    (W(1, 257, 129, 6, 2, 64, "fp16"), 0),       # G = 3: 42 positions per tile, Sq > Sk
+    (W(1, 640, 640, 4, 4, 128, causal=False), 2),
 ]
 
 
