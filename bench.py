@@ -568,6 +568,7 @@ def main():
                          "decode; splitkv: the workload through the split-KV path")
     ap.add_argument("--decode-batch", type=int, default=16, help="sequences per step for --op decode")
     ap.add_argument("--parts", type=int, default=4, help="partial states for --op merge")
+    ap.add_argument("--head-dim", type=int, default=0, help="override the workload's head dimension (64/128/256)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[x.name for x in WORKLOADS])
     ap.add_argument("--cpu-budget", type=float, default=18.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -575,6 +576,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = by_name(args.workload)
+    if args.head_dim:
+        w = w.with_sizes(D=args.head_dim, name=f"{w.name}_d{args.head_dim}")
     if args.impl == "reference":
         rank, res = run_reference(args, w)
     elif args.op == "merge":

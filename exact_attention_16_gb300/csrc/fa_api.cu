@@ -14,6 +14,14 @@
 #include "../../include/fa.h"
 #include "fa_fwd_kernel.cuh"
 
+namespace fa {
+int decode_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk, int Hq,
+                  int Hkv, int D, const long long* qs, const long long* ks, const long long* vs, const long long* os,
+                  float scale, int causal, int dtype, int num_splits, float* o_part, float* lse_part,
+                  unsigned long long workspace_bytes, cudaStream_t stream, int* status_word);
+int* current_status_word();
+}  // namespace fa
+
 namespace {
 
 __device__ int g_fa_status = 0;
@@ -161,7 +169,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (D == 256 && Hq / Hkv > 128) return FA_ERR_UNSUPPORTED;
   if (!q || !o || (Sk > 0 && (!k || !v))) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(o, 16) || (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))) ||
       (lse && !aligned(lse, 4)))
@@ -182,6 +191,15 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     fa_fill_empty_kernel<<<ds->num_sms * 4, 256, 0, stream>>>(static_cast<uint4*>(o), rows, D / 8, Sq, Hq, os[0],
                                                                 os[1], os[2], lse, n_lse);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  if (D == 256) {
+    // Two 128-row tiles with D = 256 accumulators do not fit tensor memory:
+    // the one-tile split-KV kernel runs with a single key range (no workspace).
+    int* status = fa::current_status_word();
+    if (!status) return FA_ERR_CUDA;
+    return fa::decode_launch(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, qs, ks, vs, os, scale, causal, dtype, 1, nullptr,
+                             nullptr, 0, stream, status);
   }
 
   fa::FwdParams p{};

@@ -65,7 +65,7 @@ int check_args(int B, int Sq, int Sk, int Hq, int Hkv, int D, int dtype) {
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 128) return FA_ERR_UNSUPPORTED;   // one query position of a whole group must fit a tile
   return FA_OK;
 }
@@ -102,22 +102,26 @@ unsigned long long timeout_ns() {
 namespace fa {
 
 // Launch on a given workspace (o_part / lse_part only read when n_splits > 1).
+// qs, ks, vs, os: (b, s, h) element strides (16-byte multiples, already
+// checked); the workspace layout is always contiguous.
 int decode_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk, int Hq,
-                  int Hkv, int D, float scale, int causal, int dtype, int num_splits, float* o_part, float* lse_part,
+                  int Hkv, int D, const long long* qs, const long long* ks, const long long* vs, const long long* os,
+                  float scale, int causal, int dtype, int num_splits, float* o_part, float* lse_part,
                   unsigned long long workspace_bytes, cudaStream_t stream, int* status_word) {
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const Plan pl = make_plan(B, Sq, Sk, Hq, Hkv, D, num_splits, device_sms());
   if (pl.n_splits > 1 && (workspace_bytes < pl.workspace_bytes() || !o_part || !lse_part)) return FA_ERR_INVALID_ARG;
-  const long long sq[3] = {static_cast<long long>(Sq) * Hq * D, static_cast<long long>(Hq) * D, D};
-  const long long skv[3] = {static_cast<long long>(Sk) * Hkv * D, static_cast<long long>(Hkv) * D, D};
   const int G = Hq / Hkv;
   CUtensorMap tq, tk, tv;
-  if (!encode_bshd_box(&tq, q, bf16, B, Sq, Hq, D, sq, G, pl.positions) ||
-      !encode_bshd_box(&tk, k, bf16, B, Sk, Hkv, D, skv, 1, 128) ||
-      !encode_bshd_box(&tv, v, bf16, B, Sk, Hkv, D, skv, 1, 128))
+  if (!encode_bshd_box(&tq, q, bf16, B, Sq, Hq, D, qs, G, pl.positions) ||
+      !encode_bshd_box(&tk, k, bf16, B, Sk, Hkv, D, ks, 1, 128) ||
+      !encode_bshd_box(&tv, v, bf16, B, Sk, Hkv, D, vs, 1, 128))
     return FA_ERR_CUDA;
   DecodeParams p{};
   p.o = o;
+  p.o_sb = os[0];
+  p.o_ss = os[1];
+  p.o_sh = os[2];
   p.lse = lse;
   p.o_part = o_part;
   p.lse_part = lse_part;
@@ -133,10 +137,16 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   const long long gx = static_cast<long long>(pl.n_splits) * pl.n_row_tiles;
   if (gx > 0x7fffffffLL || Hkv > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(gx), Hkv, B);
-  int rc = D == 128 ? (bf16 ? launch_decode<128, true>(tq, tk, tv, p, grid, stream)
-                            : launch_decode<128, false>(tq, tk, tv, p, grid, stream))
-                    : (bf16 ? launch_decode<64, true>(tq, tk, tv, p, grid, stream)
-                            : launch_decode<64, false>(tq, tk, tv, p, grid, stream));
+  int rc;
+  if (D == 256)
+    rc = bf16 ? launch_decode<256, true>(tq, tk, tv, p, grid, stream)
+              : launch_decode<256, false>(tq, tk, tv, p, grid, stream);
+  else if (D == 128)
+    rc = bf16 ? launch_decode<128, true>(tq, tk, tv, p, grid, stream)
+              : launch_decode<128, false>(tq, tk, tv, p, grid, stream);
+  else
+    rc = bf16 ? launch_decode<64, true>(tq, tk, tv, p, grid, stream)
+              : launch_decode<64, false>(tq, tk, tv, p, grid, stream);
   if (rc != FA_OK || pl.n_splits == 1) return rc;
   return merge_f32_parts(o_part, lse_part, pl.n_splits, o, lse, B, Sq, Hq, D, dtype, stream);
 }
@@ -172,6 +182,8 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
   const Plan pl = make_plan(B, Sq, Sk, Hq, Hkv, D, num_splits, device_sms());
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.o_part_bytes) : nullptr;
-  return fa::decode_launch(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, dtype, num_splits, o_part,
-                           lse_part, workspace_bytes, reinterpret_cast<cudaStream_t>(stream_), status);
+  const long long sq[3] = {static_cast<long long>(Sq) * Hq * D, static_cast<long long>(Hq) * D, D};
+  const long long skv[3] = {static_cast<long long>(Sk) * Hkv * D, static_cast<long long>(Hkv) * D, D};
+  return fa::decode_launch(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, sq, skv, skv, sq, scale, causal, dtype, num_splits,
+                           o_part, lse_part, workspace_bytes, reinterpret_cast<cudaStream_t>(stream_), status);
 }

@@ -13,7 +13,8 @@
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (TMEM lanes 0-127,
 // row r = s_local * G + g), warp 4 TMA producer, warp 5 MMA issuer / TMEM
 // owner. Grid: x = split + n_splits * row tile, y = KV head, z = batch.
-// TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256, 256+D).
+// TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256, 256+D);
+// D = 256 fills all 512.
 #pragma once
 
 #include <cstdint>
@@ -24,7 +25,8 @@
 namespace fa {
 
 struct DecodeParams {
-  void* o;             // final O (B, Sq, Hq, D) 16-bit (one split)
+  void* o;             // final O (B, Sq, Hq, D) 16-bit (one split), element strides below
+  long long o_sb, o_ss, o_sh;
   float* lse;          // final LSE (B, Hq, Sq) or null (one split)
   float* o_part;       // (n_splits, B, Sq, Hq, D) fp32 partial O (several splits)
   float* lse_part;     // (n_splits, B, Hq, Sq) fp32 partial LSE
@@ -43,7 +45,7 @@ struct DecodeSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 128) ? 5 : 8;
+  static constexpr int kStages = (D == 256) ? 2 : (D == 128) ? 5 : 8;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -346,46 +348,56 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_p_full);
     }
-    // ---- epilogue
-    uint32_t orr[D];
+    // ---- epilogue: O~ / l in 64-column chunks, final O or fp32 partial
     bool have_o = false;
     if (ok && n > 0) {
       if ((ok = dec_wait(bar_o_full, 0, abort_flag, p))) {
         ptx::tc_fence_after();
-        if constexpr (D == 128) ptx::tmem_ld_32x32b_x128(tmem + lane_bits + 256, orr);
-        else ptx::tmem_ld_32x32b_x64(tmem + lane_bits + 256, orr);
         have_o = true;
       }
     }
     const bool live = have_o && l_exact > 0.0f;
     const float inv_l = live ? __frcp_rn(l_exact + l_corr) : 0.0f;
     const float lse = live ? (m_ref + __log2f(l_exact)) * 0.69314718055994531f : kNegInf;
-    if (row_valid && (ok || n == 0)) {
-      const long long orow = (static_cast<long long>(b) * p.Sq + s_q) * p.Hq + hq;
-      const long long lidx = (static_cast<long long>(b) * p.Hq + hq) * p.Sq + s_q;
-      if (p.n_splits == 1) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D);
+    const bool write = row_valid && (ok || n == 0);
+    const long long lidx = (static_cast<long long>(b) * p.Hq + hq) * p.Sq + s_q;
+    const long long rows_all = static_cast<long long>(p.B) * p.Sq * p.Hq;
+    const long long orow = (static_cast<long long>(b) * p.Sq + s_q) * p.Hq + hq;
+    uint16_t* ofinal = static_cast<uint16_t*>(p.o) + static_cast<long long>(b) * p.o_sb +
+                       static_cast<long long>(s_q) * p.o_ss + static_cast<long long>(hq) * p.o_sh;
+    float* opart = p.o_part + (split * rows_all + orow) * D;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 64) {
+      uint32_t oc[64];
+      if (have_o) ptx::tmem_ld_32x32b_x64(tmem + lane_bits + 256 + c0, oc);   // whole warp
+      if (write && p.n_splits == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(ofinal + c0);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
+        for (int c = 0; c < 8; ++c) {
           float x[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) x[q] = live ? __uint_as_float(orr[8 * c + q]) * inv_l : 0.0f;
+          for (int q = 0; q < 8; ++q) x[q] = live ? __uint_as_float(oc[8 * c + q]) * inv_l : 0.0f;
           dst[c] = make_uint4(dec_pack2<BF16>(x[0], x[1]), dec_pack2<BF16>(x[2], x[3]), dec_pack2<BF16>(x[4], x[5]),
                               dec_pack2<BF16>(x[6], x[7]));
         }
-        if (p.lse) p.lse[lidx] = lse;
-      } else {
-        const long long rows_all = static_cast<long long>(p.B) * p.Sq * p.Hq;
-        float4* dst = reinterpret_cast<float4*>(p.o_part + (split * rows_all + orow) * D);
+      } else if (write) {
+        float4* dst = reinterpret_cast<float4*>(opart + c0);
 #pragma unroll
-        for (int c = 0; c < D / 4; ++c) {
+        for (int c = 0; c < 16; ++c) {
           float4 v;
-          v.x = live ? __uint_as_float(orr[4 * c + 0]) * inv_l : 0.0f;
-          v.y = live ? __uint_as_float(orr[4 * c + 1]) * inv_l : 0.0f;
-          v.z = live ? __uint_as_float(orr[4 * c + 2]) * inv_l : 0.0f;
-          v.w = live ? __uint_as_float(orr[4 * c + 3]) * inv_l : 0.0f;
+          v.x = live ? __uint_as_float(oc[4 * c + 0]) * inv_l : 0.0f;
+          v.y = live ? __uint_as_float(oc[4 * c + 1]) * inv_l : 0.0f;
+          v.z = live ? __uint_as_float(oc[4 * c + 2]) * inv_l : 0.0f;
+          v.w = live ? __uint_as_float(oc[4 * c + 3]) * inv_l : 0.0f;
           dst[c] = v;
         }
+      }
+      __syncwarp();
+    }
+    if (write) {
+      if (p.n_splits == 1) {
+        if (p.lse) p.lse[lidx] = lse;
+      } else {
         p.lse_part[split * rows_all + lidx] = lse;
       }
     }

@@ -73,7 +73,8 @@ def _call(lib, **kw):
     (dict(v=8), api.FA_ERR_INVALID_ARG),
     (dict(lse=2), api.FA_ERR_INVALID_ARG),      # not 4-byte aligned
     (dict(D=96), api.FA_ERR_UNSUPPORTED),
-    (dict(D=256), api.FA_ERR_UNSUPPORTED),
+    (dict(D=32), api.FA_ERR_UNSUPPORTED),
+    (dict(D=256, Hq=258, Hkv=1), api.FA_ERR_UNSUPPORTED),   # D = 256 takes at most 128 heads per KV head
     (dict(B=0), api.FA_OK),                     # nothing to do: no device call
     (dict(Sq=0), api.FA_OK),
     (dict(Hq=0, Hkv=1), api.FA_OK),

@@ -41,6 +41,8 @@ CASES = [
     (W(2, 300, 333, 8, 2, 128), 3),              # G = 4: 32 positions per tile, ragged
     (W(1, 257, 129, 6, 2, 64, "fp16"), 0),       # G = 3: 42 positions per tile, Sq > Sk
     (W(1, 640, 640, 4, 4, 128, causal=False), 2),
+    (W(2, 1, 2000, 16, 2, 256), 0),              # D = 256 decode, splits merged
+    (W(1, 70, 900, 8, 4, 256, "fp16"), 4),
 ]
 
 

@@ -47,6 +47,9 @@ SMALL = [
     W(1, 1000, 1000, 4, 1, 128, "fp16", causal=True, sigma=2.0),
     W(1, 640, 384, 4, 1, 128, causal=True),          # G = 4
     W(1, 129, 1000, 32, 4, 128, causal=False),       # G = 8
+    W(1, 384, 384, 4, 2, 256, causal=True),          # D = 256 (one-tile kernel, one key range)
+    W(2, 200, 333, 4, 4, 256, "fp16", causal=False),
+    W(1, 300, 257, 8, 1, 256, causal=True),          # D = 256, G = 8, Sq > Sk
 ]
 
 
@@ -139,3 +142,15 @@ def test_packed_qkv_views():
     o, lse = api.fa_fwd(q, k, v, causal=False)
     assert api.fa_status() == 0
     _oracle_compare(qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2], o, lse, D ** -0.5, False)
+
+
+def test_d256_strided_bhsd():
+    from exact_attention_16_gb300.workloads import draw_inputs
+    w = W(1, 250, 260, 4, 2, 256, causal=True, seed=13)
+    q, k, v = draw_inputs(w)
+    qb, kb, vb = (t.transpose(1, 2).contiguous().cuda() for t in (q, k, v))
+    o_store = torch.full((w.B, w.Hq, w.Sq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o, lse = api.fa_fwd(qb.transpose(1, 2), kb.transpose(1, 2), vb.transpose(1, 2), scale=w.scale, causal=True,
+                        out=o_store.transpose(1, 2))
+    assert api.fa_status() == 0
+    _oracle_compare(q, k, v, o, lse, w.scale, True)
