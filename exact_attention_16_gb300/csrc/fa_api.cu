@@ -169,8 +169,12 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
-  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
-  if (D == 256 && Hq / Hkv > 128) return FA_ERR_UNSUPPORTED;
+  if (D < 16 || D > 256 || D % 16 != 0) return FA_ERR_UNSUPPORTED;
+  // the kernel's head dimension: the smallest of 64, 128, 256 that holds D;
+  // tensor maps carry the true D, so the padding is zero-filled on load and
+  // clipped on store
+  const int Dk = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
+  if (Dk == 256 && Hq / Hkv > 128) return FA_ERR_UNSUPPORTED;
   if (!q || !o || (Sk > 0 && (!k || !v))) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(o, 16) || (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))) ||
       (lse && !aligned(lse, 4)))
@@ -193,7 +197,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
 
-  if (D == 256) {
+  if (Dk == 256) {
     // Two 128-row tiles with D = 256 accumulators do not fit tensor memory:
     // the one-tile split-KV kernel runs with a single key range (no workspace).
     int* status = fa::current_status_word();
@@ -207,6 +211,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.o_sb = os[0];
   p.o_ss = os[1];
   p.o_sh = os[2];
+  p.d_true = D;
   p.lse = lse;
   p.B = B;
   p.Sq = Sq;
@@ -235,7 +240,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     return FA_ERR_CUDA;
 
   const int grid = static_cast<int>(std::min<long long>(items, ds->num_sms));
-  if (D == 128) {
+  if (Dk == 128) {
     return bf16 ? launch<128, true>(tq, tk, tv, to, p, grid, stream)
                 : launch<128, false>(tq, tk, tv, to, p, grid, stream);
   }

@@ -65,7 +65,7 @@ int check_args(int B, int Sq, int Sk, int Hq, int Hkv, int D, int dtype) {
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
-  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (D < 16 || D > 256 || D % 16 != 0) return FA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 128) return FA_ERR_UNSUPPORTED;   // one query position of a whole group must fit a tile
   return FA_OK;
 }
@@ -122,6 +122,7 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   p.o_sb = os[0];
   p.o_ss = os[1];
   p.o_sh = os[2];
+  p.d_true = D;
   p.lse = lse;
   p.o_part = o_part;
   p.lse_part = lse_part;
@@ -137,11 +138,13 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   const long long gx = static_cast<long long>(pl.n_splits) * pl.n_row_tiles;
   if (gx > 0x7fffffffLL || Hkv > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(gx), Hkv, B);
+  // the kernel's head dimension: the smallest of 64, 128, 256 that holds D
+  const int Dk = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   int rc;
-  if (D == 256)
+  if (Dk == 256)
     rc = bf16 ? launch_decode<256, true>(tq, tk, tv, p, grid, stream)
               : launch_decode<256, false>(tq, tk, tv, p, grid, stream);
-  else if (D == 128)
+  else if (Dk == 128)
     rc = bf16 ? launch_decode<128, true>(tq, tk, tv, p, grid, stream)
               : launch_decode<128, false>(tq, tk, tv, p, grid, stream);
   else

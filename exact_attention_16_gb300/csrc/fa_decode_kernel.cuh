@@ -27,6 +27,7 @@ namespace fa {
 struct DecodeParams {
   void* o;             // final O (B, Sq, Hq, D) 16-bit (one split), element strides below
   long long o_sb, o_ss, o_sh;
+  int d_true;          // head dimension of the tensors (<= D, a multiple of 16; the tile is zero padded)
   float* lse;          // final LSE (B, Hq, Sq) or null (one split)
   float* o_part;       // (n_splits, B, Sq, Hq, D) fp32 partial O (several splits)
   float* lse_part;     // (n_splits, B, Hq, Sq) fp32 partial LSE
@@ -365,15 +366,16 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const long long orow = (static_cast<long long>(b) * p.Sq + s_q) * p.Hq + hq;
     uint16_t* ofinal = static_cast<uint16_t*>(p.o) + static_cast<long long>(b) * p.o_sb +
                        static_cast<long long>(s_q) * p.o_ss + static_cast<long long>(hq) * p.o_sh;
-    float* opart = p.o_part + (split * rows_all + orow) * D;
+    float* opart = p.o_part + (split * rows_all + orow) * p.d_true;
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 64) {
+    for (int c0 = 0; c0 < p.d_true; c0 += 64) {
       uint32_t oc[64];
       if (have_o) ptx::tmem_ld_32x32b_x64(tmem + lane_bits + 256 + c0, oc);   // whole warp
       if (write && p.n_splits == 1) {
         uint4* dst = reinterpret_cast<uint4*>(ofinal + c0);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
+          if (c0 + 8 * c >= p.d_true) break;
           float x[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) x[q] = live ? __uint_as_float(oc[8 * c + q]) * inv_l : 0.0f;
@@ -384,6 +386,7 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         float4* dst = reinterpret_cast<float4*>(opart + c0);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
+          if (c0 + 4 * c >= p.d_true) break;
           float4 v;
           v.x = live ? __uint_as_float(oc[4 * c + 0]) * inv_l : 0.0f;
           v.y = live ? __uint_as_float(oc[4 * c + 1]) * inv_l : 0.0f;

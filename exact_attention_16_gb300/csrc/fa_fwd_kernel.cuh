@@ -42,6 +42,7 @@ enum : int { kStatusOk = 0, kStatusTimeout = 4 };
 struct FwdParams {
   void* o;               // (B, Sq, Hq, D) 16-bit, element strides below, d contiguous
   long long o_sb, o_ss, o_sh;
+  int d_true;            // head dimension of the tensors (<= D, a multiple of 16; the tile is zero padded)
   float* lse;            // (B, Hq, Sq) fp32 natural log, contiguous, may be null
   int B, Sq, Sk, Hq, Hkv, group;
   int causal;
@@ -447,7 +448,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (row_valid) {
           uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int c = 0; c < D * 2 / 16; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+          for (int c = 0; c < p.d_true * 2 / 16; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
           if (p.lse) p.lse[(static_cast<long long>(w.b) * p.Hq + hq) * p.Sq + i] = -__int_as_float(0x7f800000);
         }
         continue;

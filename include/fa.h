@@ -52,9 +52,12 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype_t;
  * lse  device pointer, (B, Hq, Sq) contiguous float32 (natural log), or NULL
  *      to skip it. Rows that see no key get O = 0 and LSE = -inf.
  * B, Sq, Sk, Hq, Hkv, D   sizes; Hq must be a multiple of Hkv (query head h
- *      reads key/value head h / (Hq / Hkv)); D must be 64, 128 or 256. With
- *      D = 256 the call runs the one-tile kernel of fa_fwd_decode with a
- *      single key range (no workspace) and needs Hq / Hkv <= 128.
+ *      reads key/value head h / (Hq / Hkv)); D must be a multiple of 16 from
+ *      16 to 256. The kernels work on D = 64, 128 or 256: a smaller D runs
+ *      on the next one with the head dimension zero padded on load (no
+ *      effect on the result, extra arithmetic). D > 128 runs the one-tile
+ *      kernel of fa_fwd_decode with a single key range (no workspace) and
+ *      needs Hq / Hkv <= 128.
  * scale  softmax scale (1/sqrt(D) in the usual case); finite and > 0.
  * causal 0: every key is visible; 1: bottom-right causal mask, query i sees
  *      key j iff j <= i + Sk - Sq (top-left when Sq == Sk).
@@ -68,7 +71,7 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype_t;
  * Errors: arguments are checked before anything is enqueued. Negative sizes,
  * NULL pointers, Hkv == 0 or Hq % Hkv != 0, a non-finite or non-positive
  * scale, causal not in {0,1}, dtype not in {0,1} or a misaligned pointer give
- * FA_ERR_INVALID_ARG; D not in {64, 128, 256} or sizes whose element offsets do not
+ * FA_ERR_INVALID_ARG; D outside 16..256 or not a multiple of 16, or sizes whose element offsets do not
  * fit the kernel's 32-bit tile coordinates give FA_ERR_UNSUPPORTED. With
  * B, Sq or Hq equal to 0 nothing is written and FA_OK is returned. Sk == 0 is
  * valid: O = 0 and LSE = -inf. A failed launch returns FA_ERR_CUDA. The call

@@ -72,8 +72,9 @@ def _call(lib, **kw):
     (dict(q=24), api.FA_ERR_INVALID_ARG),       # not 16-byte aligned
     (dict(v=8), api.FA_ERR_INVALID_ARG),
     (dict(lse=2), api.FA_ERR_INVALID_ARG),      # not 4-byte aligned
-    (dict(D=96), api.FA_ERR_UNSUPPORTED),
-    (dict(D=32), api.FA_ERR_UNSUPPORTED),
+    (dict(D=40), api.FA_ERR_UNSUPPORTED),    # not a multiple of 16
+    (dict(D=8), api.FA_ERR_UNSUPPORTED),
+    (dict(D=272), api.FA_ERR_UNSUPPORTED),
     (dict(D=256, Hq=258, Hkv=1), api.FA_ERR_UNSUPPORTED),   # D = 256 takes at most 128 heads per KV head
     (dict(B=0), api.FA_OK),                     # nothing to do: no device call
     (dict(Sq=0), api.FA_OK),
@@ -84,7 +85,7 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib, kw, code):
 
 
 def test_sk_zero_needs_no_kv_pointers_but_still_validates(lib):
-    assert _call(lib, Sk=0, k=None, v=None, D=96) == api.FA_ERR_UNSUPPORTED
+    assert _call(lib, Sk=0, k=None, v=None, D=72) == api.FA_ERR_UNSUPPORTED
 
 
 def test_debug_fault_hook_validates(lib):
@@ -151,7 +152,7 @@ def test_decode_workspace_size_formula(lib):
 @pytest.mark.parametrize("args,code", [
     ((1, 17, 100, 256, 1, 128, 0), api.FA_ERR_UNSUPPORTED),   # 256 query heads per KV head > 128 rows
     ((1, 1, 100, 6, 4, 128, 0), api.FA_ERR_INVALID_ARG),      # Hq not a multiple of Hkv
-    ((1, 1, 100, 8, 8, 96, 0), api.FA_ERR_UNSUPPORTED),       # D
+    ((1, 1, 100, 8, 8, 72, 0), api.FA_ERR_UNSUPPORTED),       # D not a multiple of 16
 ])
 def test_decode_size_checks(lib, args, code):
     out = ctypes.c_ulonglong(0)

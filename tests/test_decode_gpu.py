@@ -43,6 +43,9 @@ CASES = [
     (W(1, 640, 640, 4, 4, 128, causal=False), 2),
     (W(2, 1, 2000, 16, 2, 256), 0),              # D = 256 decode, splits merged
     (W(1, 70, 900, 8, 4, 256, "fp16"), 4),
+    (W(2, 1, 1500, 16, 2, 96), 0),               # padded head dims through the split path
+    (W(1, 3, 700, 8, 8, 32, "fp16"), 3),
+    (W(1, 1, 600, 4, 4, 160), 2),
 ]
 
 

@@ -154,3 +154,30 @@ def test_d256_strided_bhsd():
                         out=o_store.transpose(1, 2))
     assert api.fa_status() == 0
     _oracle_compare(q, k, v, o, lse, w.scale, True)
+
+
+PADDED_D = [
+    W(1, 300, 257, 4, 2, 32, causal=True),           # kernel D 64, zero padded
+    W(1, 200, 200, 2, 2, 16, "fp16", causal=False),
+    W(2, 130, 190, 4, 4, 48, causal=True),
+    W(1, 257, 300, 8, 2, 96, causal=True),           # kernel D 128
+    W(1, 256, 256, 4, 1, 80, "fp16", causal=False),
+    W(1, 129, 129, 2, 2, 112, causal=True),
+    W(1, 200, 211, 4, 2, 160, causal=True),          # kernel D 256 (one-tile path)
+    W(1, 150, 150, 2, 2, 192, "fp16", causal=False),
+]
+
+
+@pytest.mark.parametrize("w", PADDED_D, ids=lambda w: f"D{w.D}_{w.dtype}_{'c' if w.causal else 'n'}_Sq{w.Sq}_Sk{w.Sk}")
+def test_head_dims_padded_to_the_kernel_tile(w):
+    check_full(w)
+
+
+def test_padded_head_dim_strided_bhsd():
+    from exact_attention_16_gb300.workloads import draw_inputs
+    w = W(1, 220, 230, 4, 2, 96, causal=True, seed=14)
+    q, k, v = draw_inputs(w)
+    qb, kb, vb = (t.transpose(1, 2).contiguous().cuda() for t in (q, k, v))
+    o, lse = api.fa_fwd(qb.transpose(1, 2), kb.transpose(1, 2), vb.transpose(1, 2), scale=w.scale, causal=True)
+    assert api.fa_status() == 0
+    _oracle_compare(q, k, v, o, lse, w.scale, True)
