@@ -9,6 +9,7 @@ hand-written CUDA kernel of ``csrc/``; see ``include/fa.h`` for the ABI.
 from .api import (  # noqa: F401
     FAError,
     fa_debug_set_fault,
+    fa_debug_set_schedule,
     fa_fwd,
     fa_fwd_strided,
     fa_merge,

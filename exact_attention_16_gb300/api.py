@@ -28,6 +28,8 @@ __all__ = [
     "fa_status_string",
     "fa_version",
     "fa_debug_set_fault",
+    "fa_debug_set_schedule",
+    "fa_fwd_schedule",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -47,10 +49,10 @@ EXPORTED_SYMBOLS = {
                               ctypes.c_void_p]),
     "fa_fwd_strided": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                      ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong),
-                                      ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
-                                      ctypes.POINTER(ctypes.c_longlong), ctypes.c_float, ctypes.c_int, ctypes.c_int,
-                                      ctypes.c_void_p]),
+                                      ctypes.c_int, ctypes.c_int,
+                                      # four `const long long[3]` stride arrays, passed by address
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fa_merge": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -68,6 +70,8 @@ EXPORTED_SYMBOLS = {
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_version": (ctypes.c_int, []),
     "fa_debug_set_fault": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "fa_debug_set_schedule": (ctypes.c_int, [ctypes.c_int]),
+    "fa_fwd_schedule": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)]),
 }
 
 
@@ -100,12 +104,32 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device_index=None):
+    """cudaStream_t of ``stream``, or of the current stream of the device."""
     import torch
 
     if stream is None:
-        stream = torch.cuda.current_stream()
+        if device_index is None:
+            device_index = torch.cuda.current_device()
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)   # cheap path, no Stream object
+        if raw is not None:
+            return ctypes.c_void_p(raw(device_index))
+        stream = torch.cuda.current_stream(device_index)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call_on(device_index, fn):
+    """Runs ``fn`` with CUDA device ``device_index`` current (switching only
+    when another device is)."""
+    import torch
+
+    if torch.cuda.current_device() == device_index:
+        return fn()
+    with torch.cuda.device(device_index):
+        return fn()
+
+
+_LL12 = ctypes.c_longlong * 12
 
 
 def _dtype_code(t):
@@ -116,10 +140,6 @@ def _dtype_code(t):
     if t.dtype == torch.float16:
         return FA_DTYPE_FP16
     raise TypeError(f"unsupported dtype {t.dtype}; expected torch.bfloat16 or torch.float16")
-
-
-def _bsh_strides(t):
-    return (ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2))
 
 
 def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=True, stream=None):
@@ -163,12 +183,14 @@ def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=
     elif lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32
                               or lse.device != q.device or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous float32 (B, Hq, Sq) tensor on q's device")
-    with torch.cuda.device(q.device):
-        rc = lib().fa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                  lse.data_ptr() if lse is not None else None,
-                                  B, Sq, Sk, Hq, Hkv, D, _bsh_strides(q), _bsh_strides(k), _bsh_strides(v),
-                                  _bsh_strides(out), float(scale), int(bool(causal)), code,
-                                  _stream_handle(stream))
+    sq, sk, sv, so = q.stride(), k.stride(), v.stride(), out.stride()
+    st = _LL12(sq[0], sq[1], sq[2], sk[0], sk[1], sk[2], sv[0], sv[1], sv[2], so[0], so[1], so[2])
+    a = ctypes.addressof(st)   # `st` stays alive until the call returns
+    dev = q.get_device()
+    rc = _call_on(dev, lambda: lib().fa_fwd_strided(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+        B, Sq, Sk, Hq, Hkv, D, a, a + 24, a + 48, a + 72, float(scale), int(bool(causal)), code,
+        _stream_handle(stream, dev)))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
     return out, lse
@@ -303,3 +325,18 @@ def fa_version() -> int:
 def fa_debug_set_fault(skip_load: int, timeout_ms: int = 0) -> int:
     """Test hook: drop K/V load ``skip_load`` of every CTA (-1 = off)."""
     return int(lib().fa_debug_set_fault(int(skip_load), int(timeout_ms)))
+
+
+def fa_fwd_schedule(B: int, Sq: int, Sk: int, Hq: int, Hkv: int, causal: bool, num_sms: int) -> int:
+    """1 if fa_fwd would run key-split items for these sizes, 0 for row-tile pairs (host only)."""
+    out = ctypes.c_int(-1)
+    rc = lib().fa_fwd_schedule(int(B), int(Sq), int(Sk), int(Hq), int(Hkv), int(causal), int(num_sms),
+                               ctypes.byref(out))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_schedule")
+    return int(out.value)
+
+
+def fa_debug_set_schedule(mode: int) -> int:
+    """Test hook: -1 cost model (default), 0 row-tile pairs, 1 key-split items."""
+    return int(lib().fa_debug_set_schedule(int(mode)))

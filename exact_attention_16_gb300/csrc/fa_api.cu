@@ -53,6 +53,7 @@ DeviceState g_dev[kMaxDevices];
 
 std::atomic<int> g_fault_skip_load{-1};
 std::atomic<int> g_fault_timeout_ms{0};
+std::atomic<int> g_schedule_mode{-1};   // -1 cost model, 0 row-tile pairs, 1 key-split
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -71,7 +72,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool KSPLIT>
 cudaError_t set_smem_attr() {
   static std::once_flag f[kMaxDevices];
   static cudaError_t err[kMaxDevices];
@@ -79,7 +80,7 @@ cudaError_t set_smem_attr() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::call_once(f[dev], [&] {
-    err[dev] = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err[dev] = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, BF16, KSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     fa::Smem<D>::kAlloc);
   });
   return err[dev];
@@ -133,10 +134,68 @@ unsigned long long wait_timeout_ns() {
 
 template <int D, bool BF16>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-           const fa::FwdParams& p, int grid, cudaStream_t stream) {
-  if (set_smem_attr<D, BF16>() != cudaSuccess) return FA_ERR_CUDA;
-  fa::fa_fwd_kernel<D, BF16><<<grid, fa::kThreads, fa::Smem<D>::kAlloc, stream>>>(tq, tk, tv, to, p);
+           const fa::FwdParams& p, bool ksplit, int grid, cudaStream_t stream) {
+  if (ksplit) {
+    if (set_smem_attr<D, BF16, true>() != cudaSuccess) return FA_ERR_CUDA;
+    fa::fa_fwd_kernel<D, BF16, true><<<grid, fa::kThreads, fa::Smem<D>::kAlloc, stream>>>(tq, tk, tv, to, p);
+  } else {
+    if (set_smem_attr<D, BF16, false>() != cudaSuccess) return FA_ERR_CUDA;
+    fa::fa_fwd_kernel<D, BF16, false><<<grid, fa::kThreads, fa::Smem<D>::kAlloc, stream>>>(tq, tk, tv, to, p);
+  }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Work items of each schedule: row-tile pairs (two heads of a GQA group, or
+// two row tiles of one head) or key-split single row tiles.
+void set_items(fa::FwdParams& p, bool ksplit) {
+  p.pair_heads = (!ksplit && p.group % 2 == 0) ? 1 : 0;
+  p.n_units = p.pair_heads ? p.Hq / 2 : p.Hq;
+  p.n_mslots = (ksplit || p.pair_heads) ? p.n_mtiles : (p.n_mtiles + 1) / 2;
+}
+
+// Finishing time of the busiest CTA under the static serpentine schedule, in
+// key-tile steps (one step = one key tile for both slots of a CTA). A key-split
+// item of n key tiles takes ceil(n / 2) steps, each 1.3 times as long as a
+// row-tile-pair step (every K/V tile feeds one slot instead of two); every
+// item also pays 1.75 steps of Q load, pipeline fill and epilogue. Both
+// constants are fitted to GB300 timings of 18 shapes (MHA and GQA, causal and
+// not, 0.5K to 32K keys), on which the model picks the faster schedule every
+// time and predicts the time ratio within 6 %.
+double schedule_makespan(const fa::FwdParams& p, bool ksplit, int grid) {
+  constexpr double kItemOverhead = 1.75;
+  constexpr double kSplitStep = 1.3;
+  const int n_items = p.n_items;
+  double worst = 0.0;
+  for (int cta = 0; cta < grid; ++cta) {
+    double t = 0.0;
+    for (int round = 0; round * grid < n_items; ++round) {
+      const int idx = fa::item_of_round(round, cta, grid);
+      if (idx >= n_items) continue;
+      const int n = ksplit ? fa::decode_item<true>(p, idx).n_kv : fa::decode_item<false>(p, idx).n_kv;
+      if (n == 0) continue;
+      t += (ksplit ? kSplitStep * ((n + 1) / 2) : n) + kItemOverhead;
+    }
+    worst = std::max(worst, t);
+  }
+  return worst;
+}
+
+// Picks key-split items when the row-tile pairs would leave SMs idle: too few
+// items for the grid, or a long causal tail. Large problems (many waves) keep
+// the pairs, whose shared K/V tiles halve the loads per MMA.
+bool use_key_split(fa::FwdParams& p, int num_sms) {
+  const int mode = g_schedule_mode.load();
+  if (mode == 0 || mode == 1) return mode == 1;
+  set_items(p, false);
+  const long long pair_items = static_cast<long long>(p.B) * p.n_units * p.n_mslots;
+  if (pair_items > 4LL * num_sms) return false;
+  p.n_items = static_cast<int>(pair_items);
+  const double t_pair = schedule_makespan(p, false, static_cast<int>(std::min<long long>(pair_items, num_sms)));
+  set_items(p, true);
+  const long long split_items = static_cast<long long>(p.B) * p.n_units * p.n_mslots;
+  p.n_items = static_cast<int>(split_items);
+  const double t_split = schedule_makespan(p, true, static_cast<int>(std::min<long long>(split_items, num_sms)));
+  return t_split < t_pair;
 }
 
 }  // namespace
@@ -223,11 +282,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.n_mtiles = (Sq + fa::kBM - 1) / fa::kBM;
   p.n_kv_tiles = (Sk + fa::kBN - 1) / fa::kBN;
-  p.pair_heads = (p.group % 2 == 0) ? 1 : 0;
-  p.n_units = p.pair_heads ? Hq / 2 : Hq;
-  p.n_mslots = p.pair_heads ? p.n_mtiles : (p.n_mtiles + 1) / 2;
+  // every item count below fits an int: B * Hq * ceil(Sq / 128) does
+  if (static_cast<long long>(B) * Hq * p.n_mtiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const bool ksplit = use_key_split(p, ds->num_sms);
+  set_items(p, ksplit);
   const long long items = static_cast<long long>(B) * p.n_units * p.n_mslots;
-  if (items > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   p.n_items = static_cast<int>(items);
   p.timeout_ns = wait_timeout_ns();
   p.inject_skip_load = g_fault_skip_load.load();
@@ -241,10 +300,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 
   const int grid = static_cast<int>(std::min<long long>(items, ds->num_sms));
   if (Dk == 128) {
-    return bf16 ? launch<128, true>(tq, tk, tv, to, p, grid, stream)
-                : launch<128, false>(tq, tk, tv, to, p, grid, stream);
+    return bf16 ? launch<128, true>(tq, tk, tv, to, p, ksplit, grid, stream)
+                : launch<128, false>(tq, tk, tv, to, p, ksplit, grid, stream);
   }
-  return bf16 ? launch<64, true>(tq, tk, tv, to, p, grid, stream) : launch<64, false>(tq, tk, tv, to, p, grid, stream);
+  return bf16 ? launch<64, true>(tq, tk, tv, to, p, ksplit, grid, stream)
+              : launch<64, false>(tq, tk, tv, to, p, ksplit, grid, stream);
 }
 
 }  // namespace
@@ -296,6 +356,31 @@ extern "C" const char* fa_status_string(int code) {
 }
 
 extern "C" int fa_version(void) { return 100; }
+
+extern "C" int fa_fwd_schedule(int B, int Sq, int Sk, int Hq, int Hkv, int causal, int num_sms, int* key_split) {
+  if (!key_split || B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_sms <= 0 ||
+      (causal != 0 && causal != 1))
+    return FA_ERR_INVALID_ARG;
+  fa::FwdParams p{};
+  p.B = B;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = Hq / Hkv;
+  p.causal = causal;
+  p.n_mtiles = (Sq + fa::kBM - 1) / fa::kBM;
+  p.n_kv_tiles = (Sk + fa::kBN - 1) / fa::kBN;
+  if (static_cast<long long>(B) * Hq * p.n_mtiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  *key_split = use_key_split(p, num_sms) ? 1 : 0;
+  return FA_OK;
+}
+
+extern "C" int fa_debug_set_schedule(int mode) {
+  if (mode < -1 || mode > 1) return FA_ERR_INVALID_ARG;
+  g_schedule_mode.store(mode);
+  return FA_OK;
+}
 
 extern "C" int fa_debug_set_fault(int skip_load, int timeout_ms) {
   if (skip_load < -1) return FA_ERR_INVALID_ARG;

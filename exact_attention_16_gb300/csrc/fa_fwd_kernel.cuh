@@ -21,6 +21,16 @@
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // The softmax writes P (16-bit, two per column) over the first 64 columns of
 // its S region; the PV MMA reads P from TMEM and V from shared memory.
+//
+// Key-split items (KSPLIT) serve problems with too few row tiles to fill the
+// SMs, the short-sequence case of "NVIDIA闪存注意力实操" section "自动调优"
+// (large tiles leave SMs idle). A work item is then ONE 128-row query tile,
+// and its two slots run the even and the odd key tiles against the same Q.
+// Each slot keeps its own online-softmax state (m, l, O~); at the end the
+// tile-0 warps combine the two with the rescale of "MiniPaged-Qwen: Qwen3
+// Prefill FlashAttention" section 4: m = max(m0, m1), a_t = 2^(m_t - m),
+// O = (a0 O~0 + a1 O~1) / (a0 l0 + a1 l1). Twice as many items, each half as
+// long, and no workspace.
 #pragma once
 
 #include <cstdint>
@@ -72,8 +82,13 @@ struct Smem {
   static constexpr int kOStageWarpBytes = 32 * 128;
   static constexpr int kBarOff = kOStageOff + 8 * kOStageWarpBytes;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_lo[2]
-  //           p_hi[2] o_full[2] o_empty[2] teardown
-  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 2 + 1;
+  //           p_hi[2] o_full[2] o_empty[2] teardown stats_full stats_empty
+  // (key-split items ring one stage more: see the kernel)
+  static constexpr int kNumBars = 2 + 2 + (kStages + 1) + (kStages + 1) + 2 + 2 + 2 + 2 + 2 + 1 + 2;
+  // Key-split items: slot 1 hands its per-row (m, l, l_corr) to the tile-0
+  // warps in the O staging buffer of warp 4, which only slot 0 stores from
+  // otherwise (3 x 128 floats).
+  static constexpr int kStatsOff = kOStageOff + 4 * kOStageWarpBytes;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
@@ -85,10 +100,11 @@ struct WorkItem {
 };
 
 // Number of 128-key tiles query rows [r0, r0+128) need (0 if none visible).
-__device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int r0) {
+// Host code calls it too, to cost the schedule before the launch.
+__host__ __device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int r0) {
   if (r0 >= p.Sq) return 0;
   if (!p.causal) return p.n_kv_tiles;
-  int r_last = min(r0 + kBM - 1, p.Sq - 1);
+  int r_last = (r0 + kBM - 1 < p.Sq - 1) ? r0 + kBM - 1 : p.Sq - 1;
   long long lim = static_cast<long long>(r_last) + (p.Sk - p.Sq) + 1;  // exclusive key bound
   if (lim <= 0) return 0;
   if (lim > p.Sk) lim = p.Sk;
@@ -97,15 +113,22 @@ __device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int r0) {
 
 // Work items are numbered longest first: row-tile slot descending (causal
 // cost grows with the row index), then batch, then head unit, so the heads of
-// one GQA group run side by side and share K/V through L2.
-__device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int idx) {
+// one GQA group run side by side and share K/V through L2. Key-split items
+// are single row tiles (head unit = head, slot = row tile).
+template <bool KSPLIT>
+__host__ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int idx) {
   WorkItem w;
   int per_slot = p.B * p.n_units;
   int slot = p.n_mslots - 1 - idx / per_slot;
   int rem = idx % per_slot;
   w.b = rem / p.n_units;
   int unit = rem % p.n_units;
-  if (p.pair_heads) {
+  if (KSPLIT) {
+    w.hq0 = unit;
+    w.hq1 = unit;
+    w.r0 = slot * kBM;
+    w.r1 = slot * kBM;
+  } else if (p.pair_heads) {
     w.hq0 = 2 * unit;
     w.hq1 = 2 * unit + 1;
     w.r0 = slot * kBM;
@@ -117,13 +140,14 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int idx) {
     w.r1 = (2 * slot + 1) * kBM;
   }
   w.kvh = w.hq0 / p.group;
-  w.n_kv = max(kv_tiles_for(p, w.r0), kv_tiles_for(p, w.r1));
+  const int n0 = kv_tiles_for(p, w.r0), n1 = kv_tiles_for(p, w.r1);
+  w.n_kv = n0 > n1 ? n0 : n1;
   return w;
 }
 
 // Serpentine static schedule over the longest-first order: CTA c takes item
 // r*G + c on even rounds and r*G + (G-1-c) on odd rounds.
-__device__ __forceinline__ int item_of_round(int round, int cta, int grid) {
+__host__ __device__ __forceinline__ int item_of_round(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
@@ -152,13 +176,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   else return ptx::pack_f16x2(lo, hi);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool KSPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
               const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
-  constexpr int kStages = L::kStages;
+  // Key-split items load Q into slot 0 only: the slot-1 Q buffer, which sits
+  // just below the K/V ring, becomes one more ring stage.
+  constexpr int kStages = KSPLIT ? L::kStages + 1 : L::kStages;
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
 
@@ -168,7 +194,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
 
   const uint32_t sQ = base + L::kQOff;
-  const uint32_t sKV = base + L::kKVOff;
+  const uint32_t sKV = base + (KSPLIT ? L::kQOff + L::kTileBytes : L::kKVOff);
   const uint32_t bars = base + L::kBarOff;
   const uint32_t bar_q_full = bars;                       // [2]
   const uint32_t bar_q_empty = bars + 2 * 8;              // [2]
@@ -180,6 +206,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const uint32_t bar_o_full = bar_p_hi + 2 * 8;            // [2]
   const uint32_t bar_o_empty = bar_o_full + 2 * 8;         // [2]
   const uint32_t bar_teardown = bar_o_empty + 2 * 8;
+  const uint32_t bar_stats_full = bar_teardown + 8;       // key-split: slot 1 state written
+  const uint32_t bar_stats_empty = bar_teardown + 16;     // key-split: slot 1 state consumed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::kMiscOff + 4);
 
@@ -201,6 +229,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_init(bar_kv_empty + 8 * s, 1);
     }
     ptx::mbar_init(bar_teardown, 1);
+    ptx::mbar_init(bar_stats_full, 128);
+    ptx::mbar_init(bar_stats_empty, 128);
     *abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
@@ -261,27 +291,41 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int idx = item_of_round(round, cta, grid);
       if (round * grid >= p.n_items) break;
       if (idx >= p.n_items) continue;
-      const WorkItem w = decode_item(p, idx);
+      const WorkItem w = decode_item<KSPLIT>(p, idx);
       if (w.n_kv == 0) continue;
-      ok = load_q(0, w.hq0, w.r0, w.b) && load_kv(&tm_k, 0, w.kvh, w.b) && load_q(1, w.hq1, w.r1, w.b) &&
-           load_kv(&tm_v, 0, w.kvh, w.b);
+      // key-split: slot t runs key tiles t, t+2, ...; n1 of them for slot 1
+      const int n1 = w.n_kv / 2, n0 = w.n_kv - n1;
+      if constexpr (KSPLIT)
+        ok = load_q(0, w.hq0, w.r0, w.b) && load_kv(&tm_k, 0, w.kvh, w.b) &&
+             (n1 == 0 || load_kv(&tm_k, 1, w.kvh, w.b));
+      else
+        ok = load_q(0, w.hq0, w.r0, w.b) && load_kv(&tm_k, 0, w.kvh, w.b) && load_q(1, w.hq1, w.r1, w.b) &&
+             load_kv(&tm_v, 0, w.kvh, w.b);
       // Q tiles are read once from HBM: pull the next item's into L2 now so
       // that its TMA load at the item boundary hits L2.
       if (ok && lane == 0) {
         const int nidx = item_of_round(round + 1, cta, grid);
         if ((round + 1) * grid < p.n_items && nidx < p.n_items) {
-          const WorkItem nw = decode_item(p, nidx);
+          const WorkItem nw = decode_item<KSPLIT>(p, nidx);
           if (nw.n_kv > 0) {
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
               ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq0, nw.r0, nw.b);
-              ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq1, nw.r1, nw.b);
+              if (!KSPLIT) ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq1, nw.r1, nw.b);
             }
           }
         }
       }
-      for (int j = 1; ok && j < w.n_kv; ++j)
-        ok = load_kv(&tm_k, j, w.kvh, w.b) && load_kv(&tm_v, j, w.kvh, w.b);
+      if constexpr (KSPLIT) {
+        // the MMA issuer's order: V(s, 0), K(s+1, 0), V(s, 1), K(s+1, 1)
+        for (int st = 0; ok && st < n0; ++st)
+          ok = load_kv(&tm_v, 2 * st, w.kvh, w.b) && (st + 1 >= n0 || load_kv(&tm_k, 2 * st + 2, w.kvh, w.b)) &&
+               (st >= n1 || load_kv(&tm_v, 2 * st + 1, w.kvh, w.b)) &&
+               (st + 1 >= n1 || load_kv(&tm_k, 2 * st + 3, w.kvh, w.b));
+      } else {
+        for (int j = 1; ok && j < w.n_kv; ++j)
+          ok = load_kv(&tm_k, j, w.kvh, w.b) && load_kv(&tm_v, j, w.kvh, w.b);
+      }
       ++act;
     }
     if (!ok && lane == 0) {
@@ -312,7 +356,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     bool ok = true;
     // S_t = Q_t K^T: D/16 MMAs over the head dimension.
     auto issue_s = [&](int t, uint32_t st) {
-      const uint64_t a = t ? dq1 : dq0;
+      const uint64_t a = (t && !KSPLIT) ? dq1 : dq0;   // key-split: both slots read Q tile 0
       const uint64_t bk = dk0 + st * kStageDesc;
       const uint32_t d = tmem + (t ? kColS1 : kColS0);
 #pragma unroll
@@ -336,13 +380,95 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     auto wait_stage = [&](uint32_t it) -> bool {
       return bar_wait(bar_kv_full + 8 * (it % kStages), (it / kStages) & 1u, abort_flag, p);
     };
+    // O_t (+)= P_t V for one key tile, each half of P as soon as the softmax
+    // has written it.
+    auto pv_tile = [&](int t, uint32_t v_stage, bool first) -> bool {
+      if (!bar_wait(bar_p_lo + 8 * t, p_phase[t], abort_flag, p)) return false;
+      if (ptx::mbar_test_wait(bar_p_hi + 8 * t, p_phase[t])) {
+        // all of P_t is written: one run of 8 P V MMAs
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          issue_pv(t, v_stage, 0, first);
+          issue_pv(t, v_stage, 1, first);
+        }
+      } else {
+        // the softmax is still on keys 64..127: start on keys 0..63
+        ptx::tc_fence_after();
+        if (lane == 0) issue_pv(t, v_stage, 0, first);
+        __syncwarp();
+        if (!bar_wait(bar_p_hi + 8 * t, p_phase[t], abort_flag, p)) return false;
+        ptx::tc_fence_after();
+        if (lane == 0) issue_pv(t, v_stage, 1, first);
+      }
+      p_phase[t] ^= 1u;
+      return true;
+    };
     for (int round = 0; ok; ++round) {
       const int idx = item_of_round(round, cta, grid);
       if (round * grid >= p.n_items) break;
       if (idx >= p.n_items) continue;
-      const WorkItem w = decode_item(p, idx);
+      const WorkItem w = decode_item<KSPLIT>(p, idx);
       if (w.n_kv == 0) continue;
       const uint32_t par = act & 1u;
+      if constexpr (KSPLIT) {
+        // Slot t runs key tiles t, t+2, ...: S_t from its first key tile, then
+        // per step P_t V and the next S_t, each slot on its own K/V stages.
+        const int n1 = w.n_kv / 2, n0 = w.n_kv - n1;
+        int s_left = w.n_kv;   // S MMAs of this item still to issue (each reads Q)
+        if (!(ok = bar_wait(bar_q_full, par, abort_flag, p))) break;
+        for (int t = 0; ok && t < 2; ++t) {
+          if (t == 1 && n1 == 0) {
+            // slot 1 has no key tile: close its O phase without an MMA
+            if (!(ok = bar_wait(bar_o_empty + 8, par ^ 1u, abort_flag, p))) break;
+            if (lane == 0) ptx::mma_commit(bar_o_full + 8);
+            __syncwarp();
+            break;
+          }
+          const uint32_t st = kv_it % kStages;
+          if (!(ok = wait_stage(kv_it))) break;
+          ++kv_it;
+          const bool last = --s_left == 0;
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            issue_s(t, st);
+            ptx::mma_commit(bar_s_full + 8 * t);
+            ptx::mma_commit(bar_kv_empty + 8 * st);
+            if (last) ptx::mma_commit(bar_q_empty);
+          }
+          __syncwarp();
+        }
+        for (int sj = 0; ok && sj < n0; ++sj) {
+          for (int t = 0; t < 2; ++t) {
+            const int nt = t ? n1 : n0;
+            if (sj >= nt) break;
+            const uint32_t v_stage = kv_it % kStages;
+            if (!(ok = wait_stage(kv_it))) break;
+            ++kv_it;
+            if (sj == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
+            if (!(ok = pv_tile(t, v_stage, sj == 0))) break;
+            if (lane == 0) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
+            __syncwarp();
+            if (sj + 1 < nt) {
+              const uint32_t k_stage = kv_it % kStages;
+              if (!(ok = wait_stage(kv_it))) break;
+              ++kv_it;
+              const bool last = --s_left == 0;
+              ptx::tc_fence_after();
+              if (lane == 0) {
+                issue_s(t, k_stage);
+                ptx::mma_commit(bar_s_full + 8 * t);
+                ptx::mma_commit(bar_kv_empty + 8 * k_stage);
+                if (last) ptx::mma_commit(bar_q_empty);
+              }
+            } else if (lane == 0) {
+              ptx::mma_commit(bar_o_full + 8 * t);
+            }
+            __syncwarp();
+          }
+        }
+        ++act;
+        continue;
+      }
       uint32_t k_stage = kv_it % kStages;
       // prologue: S_0 = Q_0 K_0^T as soon as Q_0 and K_0 land, then S_1
       if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_stage(kv_it))) break;
@@ -379,24 +505,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         for (int t = 0; t < 2; ++t) {
           if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-          if (!(ok = bar_wait(bar_p_lo + 8 * t, p_phase[t], abort_flag, p))) break;
-          if (ptx::mbar_test_wait(bar_p_hi + 8 * t, p_phase[t])) {
-            // all of P_t(j) is written: one run of 8 P V MMAs
-            ptx::tc_fence_after();
-            if (lane == 0) {
-              issue_pv(t, v_stage, 0, j == 0);
-              issue_pv(t, v_stage, 1, j == 0);
-            }
-          } else {
-            // the softmax is still on keys 64..127: start on keys 0..63
-            ptx::tc_fence_after();
-            if (lane == 0) issue_pv(t, v_stage, 0, j == 0);
-            __syncwarp();
-            if (!(ok = bar_wait(bar_p_hi + 8 * t, p_phase[t], abort_flag, p))) break;
-            ptx::tc_fence_after();
-            if (lane == 0) issue_pv(t, v_stage, 1, j == 0);
-          }
-          p_phase[t] ^= 1u;
+          if (!(ok = pv_tile(t, v_stage, j == 0))) break;
           if (lane == 0) {
             if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
             if (more) {
@@ -436,7 +545,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int idx = item_of_round(round, cta, grid);
       if (round * grid >= p.n_items) break;
       if (idx >= p.n_items) continue;
-      const WorkItem w = decode_item(p, idx);
+      const WorkItem w = decode_item<KSPLIT>(p, idx);
       const int hq = t ? w.hq1 : w.hq0;
       const int r0 = t ? w.r1 : w.r0;
       const int i = r0 + row;                // query row index
@@ -445,7 +554,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                       (static_cast<long long>(w.b) * p.o_sb + static_cast<long long>(i) * p.o_ss +
                        static_cast<long long>(hq) * p.o_sh) * 2;
       if (w.n_kv == 0) {
-        if (row_valid) {
+        if (row_valid && !(KSPLIT && t == 1)) {   // key-split: slot 0 owns the rows
           uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int c = 0; c < p.d_true * 2 / 16; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
@@ -469,7 +578,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       float m_ref = -__int_as_float(0x7f800000);
       float l_exact = 0.0f, l_corr = 0.0f;
-      for (int j = 0; j < w.n_kv; ++j) {
+      // key-split: this slot's key tiles are t, t+2, ...
+      const int n_mine = KSPLIT ? (t ? w.n_kv / 2 : w.n_kv - w.n_kv / 2) : w.n_kv;
+      for (int sj = 0; sj < n_mine; ++sj) {
+        const int j = KSPLIT ? 2 * sj + t : sj;   // key tile
         if (!(ok = bar_wait(bar_s_full + 8 * t, s_phase, abort_flag, p))) break;
         s_phase ^= 1u;
         ptx::tc_fence_after();
@@ -543,7 +655,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         // Rescale O~ when some row of this warp raised its reference max. The
         // previous P V of this tile completed before S of this key tile did.
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (sj > 0 && __any_sync(0xffffffffu, need)) {
           const uint64_t a2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -578,6 +690,83 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::mbar_arrive(bar_p_hi + 8 * t);
       }
       if (!ok) break;
+      if constexpr (KSPLIT) {
+        // ---- key-split epilogue: slot 1 hands (m, l, l_corr) to slot 0, which
+        // combines both slots' states and stores O and LSE
+        float* stats = reinterpret_cast<float*>(base_ptr + L::kStatsOff);
+        if (t == 1) {
+          if (!(ok = bar_wait(bar_stats_empty, (act & 1u) ^ 1u, abort_flag, p))) break;
+          stats[row] = m_ref;
+          stats[kBM + row] = l_exact;
+          stats[2 * kBM + row] = l_corr;
+          ptx::mbar_arrive(bar_stats_full);
+          ++act;
+          continue;
+        }
+        if (!(ok = bar_wait(bar_stats_full, act & 1u, abort_flag, p))) break;
+        const float m1 = stats[row], l1 = stats[kBM + row], c1 = stats[2 * kBM + row];
+        ptx::mbar_arrive(bar_stats_empty);
+        // a slot with l > 0 has a finite m; one with l = 0 contributes nothing
+        const float m = l1 > 0.0f ? (l_exact > 0.0f ? fmaxf(m_ref, m1) : m1) : m_ref;
+        const float a0 = l_exact > 0.0f ? ptx::ex2_approx(m_ref - m) : 0.0f;
+        const float a1 = l1 > 0.0f ? ptx::ex2_approx(m1 - m) : 0.0f;
+        const float l_tot = a0 * l_exact + a1 * l1;
+        const bool live = l_tot > 0.0f;
+        const float inv_l = live ? __frcp_rn(a0 * (l_exact + l_corr) + a1 * (l1 + c1)) : 0.0f;
+        const uint64_t f0 = ptx::f2_pack(a0 * inv_l, a0 * inv_l);
+        const uint64_t f1 = ptx::f2_pack(a1 * inv_l, a1 * inv_l);
+        const bool has1 = w.n_kv >= 2;   // slot 1 ran at least one key tile
+        if (!(ok = bar_wait(bar_o_full, act & 1u, abort_flag, p) && bar_wait(bar_o_full + 8, act & 1u, abort_flag, p)))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t tO1 = tmem + lane_bits + kColO1;
+        const int wrow = row & 31;
+        const uint32_t stage = base + L::kOStageOff + warp * L::kOStageWarpBytes;
+#pragma unroll
+        for (int ch = 0; ch < L::kChunks; ++ch) {
+          uint32_t x0[64], x1[64];
+          ptx::tmem_ld_32x32b_x64(tO + 64 * ch, x0);
+          if (has1) {
+            ptx::tmem_ld_32x32b_x64(tO1 + 64 * ch, x1);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) x1[c] = 0u;
+          }
+          if (ch == L::kChunks - 1) {
+            // both accumulators are in registers: the MMA may reuse them
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_o_empty);
+            ptx::mbar_arrive(bar_o_empty + 8);
+          }
+          uint32_t ob[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint64_t y0 = ptx::f2_pack(__uint_as_float(x0[2 * c]), __uint_as_float(x0[2 * c + 1]));
+            const uint64_t y1 = ptx::f2_pack(__uint_as_float(x1[2 * c]), __uint_as_float(x1[2 * c + 1]));
+            float a, b;
+            ptx::f2_unpack(ptx::f2_fma(y1, f1, ptx::f2_mul(y0, f0)), a, b);
+            ob[c] = pack2<BF16>(a, b);
+          }
+          if (lane == 0) ptx::bulk_wait_group_read0();   // the previous store has read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            ptx::st_shared_v4(stage + wrow * 128 + ((k ^ (wrow & 7)) << 4), ob[4 * k], ob[4 * k + 1], ob[4 * k + 2],
+                              ob[4 * k + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_4d(&tm_o, stage, ch * 64, hq, r0 + (warp & 3) * 32, w.b);
+            ptx::bulk_commit_group();
+          }
+        }
+        if (row_valid && p.lse) {
+          const float lse = live ? (m + __log2f(l_tot)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
+          p.lse[(static_cast<long long>(w.b) * p.Hq + hq) * p.Sq + i] = lse;
+        }
+        ++act;
+        continue;
+      }
       // ---- epilogue: O = O~ / l, LSE = (m + log2 l) * ln 2
       if (!(ok = bar_wait(bar_o_full + 8 * t, act & 1u, abort_flag, p))) break;
       ptx::tc_fence_after();

@@ -196,6 +196,32 @@ int fa_version(void);
  */
 int fa_debug_set_fault(int skip_load, int timeout_ms);
 
+/*
+ * fa_fwd_schedule — the work decomposition fa_fwd would use for these sizes
+ * (head dimension <= 128) on a GPU with `num_sms` SMs, without touching any
+ * GPU: *key_split = 0 for row-tile pairs, 1 for key-split items (see
+ * fa_debug_set_schedule, whose override it reports too). Host arithmetic
+ * only: a static cost model of the persistent schedule, in key-tile steps.
+ * FA_ERR_INVALID_ARG for a null `key_split`, non-positive sizes, Hq not a
+ * multiple of Hkv or causal not 0/1.
+ */
+int fa_fwd_schedule(int B, int Sq, int Sk, int Hq, int Hkv, int causal, int num_sms, int* key_split);
+
+/*
+ * fa_debug_set_schedule — test hook that fixes the work decomposition of
+ * every later fa_fwd / fa_fwd_strided call in this process (D <= 128):
+ *   -1  (default) a host cost model picks per call;
+ *    0  row-tile pairs: each CTA work item is two 128-row query tiles that
+ *       share every K/V tile (two heads of a GQA group, or two row tiles);
+ *    1  key-split: each item is one 128-row query tile whose even and odd key
+ *       tiles run side by side and are combined before the store (more,
+ *       shorter items: the short-sequence case of "NVIDIA闪存注意力实操"
+ *       section "自动调优").
+ * The result is the same attention either way, up to rounding. Returns
+ * FA_ERR_INVALID_ARG for any other mode.
+ */
+int fa_debug_set_schedule(int mode);
+
 #ifdef __cplusplus
 }
 #endif

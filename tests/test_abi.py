@@ -93,6 +93,13 @@ def test_debug_fault_hook_validates(lib):
     assert api.fa_debug_set_fault(-1) == api.FA_OK
 
 
+def test_debug_schedule_hook_validates(lib):
+    assert api.fa_debug_set_schedule(2) == api.FA_ERR_INVALID_ARG
+    assert api.fa_debug_set_schedule(-2) == api.FA_ERR_INVALID_ARG
+    for mode in (1, 0, -1):
+        assert api.fa_debug_set_schedule(mode) == api.FA_OK
+
+
 def _call_strided(lib, qs=None, ks=None, vs=None, os_=None, **kw):
     args = dict(q=16, k=16, v=16, o=16, lse=None, B=2, Sq=4, Sk=4, Hq=2, Hkv=1, D=128,
                 scale=0.125, causal=0, dtype=1, stream=None)

@@ -25,6 +25,7 @@ from parity import compare
 import oracle
 
 w = Workload("fault", 1, 512, 512, 2, 2, 128, "bf16", True, 1.0, 1.0, 5)
+api.fa_debug_set_schedule(int(sys.argv[2]))   # 0 row-tile pairs, 1 key-split items
 q, k, v = draw_inputs(w)
 qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
 out = {}
@@ -45,11 +46,13 @@ print("RESULT " + json.dumps(out))
 """
 
 
-def test_dropped_load_times_out_and_context_survives():
+@pytest.mark.parametrize("schedule", [0, 1], ids=["pairs", "keysplit"])
+def test_dropped_load_times_out_and_context_survives(schedule):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    proc = subprocess.run([sys.executable, "-c", CHILD, ROOT], capture_output=True, text=True, timeout=300)
+    proc = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(schedule)], capture_output=True, text=True,
+                          timeout=300)
     line = [ln for ln in proc.stdout.splitlines() if ln.startswith("RESULT ")]
     assert proc.returncode == 0 and line, proc.stdout[-2000:] + proc.stderr[-2000:]
     res = json.loads(line[0][len("RESULT "):])
