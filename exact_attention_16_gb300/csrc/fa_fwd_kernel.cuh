@@ -81,10 +81,10 @@ struct Smem {
   static constexpr int kOStageOff = kKVOff + kStages * kTileBytes;
   static constexpr int kOStageWarpBytes = 32 * 128;
   static constexpr int kBarOff = kOStageOff + 8 * kOStageWarpBytes;
-  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_lo[2]
-  //           p_hi[2] o_full[2] o_empty[2] teardown stats_full stats_empty
-  // (key-split items ring one stage more: see the kernel)
-  static constexpr int kNumBars = 2 + 2 + (kStages + 1) + (kStages + 1) + 2 + 2 + 2 + 2 + 2 + 1 + 2;
+  // barriers: q_full[2] q_empty[2] kv_full[S/2] kv_empty[S/2] s_full[2]
+  //           p_full[2] (2 unused) o_full[2] o_empty[2] teardown stats_full
+  //           stats_empty (at most this many)
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 2 + 1 + 2;
   // Key-split items: slot 1 hands its per-row (m, l, l_corr) to the tile-0
   // warps in the O staging buffer of warp 4, which only slot 0 stores from
   // otherwise (3 x 128 floats).
@@ -182,9 +182,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
               const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
-  // Key-split items load Q into slot 0 only: the slot-1 Q buffer, which sits
-  // just below the K/V ring, becomes one more ring stage.
-  constexpr int kStages = KSPLIT ? L::kStages + 1 : L::kStages;
+  constexpr int kSlots = L::kStages / 2;   // K/V ring slots of two tiles each
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
 
@@ -194,16 +192,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
 
   const uint32_t sQ = base + L::kQOff;
-  const uint32_t sKV = base + (KSPLIT ? L::kQOff + L::kTileBytes : L::kKVOff);
+  const uint32_t sKV = base + L::kKVOff;
   const uint32_t bars = base + L::kBarOff;
   const uint32_t bar_q_full = bars;                       // [2]
   const uint32_t bar_q_empty = bars + 2 * 8;              // [2]
-  const uint32_t bar_kv_full = bars + 4 * 8;              // [kStages]
-  const uint32_t bar_kv_empty = bar_kv_full + kStages * 8;
-  const uint32_t bar_s_full = bar_kv_empty + kStages * 8;  // [2]
-  const uint32_t bar_p_lo = bar_s_full + 2 * 8;            // [2] P columns 0..31 (keys 0..63) written
-  const uint32_t bar_p_hi = bar_p_lo + 2 * 8;              // [2] P columns 32..63 (keys 64..127) written
-  const uint32_t bar_o_full = bar_p_hi + 2 * 8;            // [2]
+  const uint32_t bar_kv_full = bars + 4 * 8;              // [kSlots]
+  const uint32_t bar_kv_empty = bar_kv_full + kSlots * 8;  // [kSlots]
+  const uint32_t bar_s_full = bar_kv_empty + kSlots * 8;   // [2]
+  const uint32_t bar_p_full = bar_s_full + 2 * 8;          // [2] P (all 64 columns) written
+  const uint32_t bar_o_full = bar_p_full + 4 * 8;          // [2]
   const uint32_t bar_o_empty = bar_o_full + 2 * 8;         // [2]
   const uint32_t bar_teardown = bar_o_empty + 2 * 8;
   const uint32_t bar_stats_full = bar_teardown + 8;       // key-split: slot 1 state written
@@ -219,12 +216,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_init(bar_q_full + 8 * t, 1);
       ptx::mbar_init(bar_q_empty + 8 * t, 1);
       ptx::mbar_init(bar_s_full + 8 * t, 1);
-      ptx::mbar_init(bar_p_lo + 8 * t, 128);
-      ptx::mbar_init(bar_p_hi + 8 * t, 128);
+      ptx::mbar_init(bar_p_full + 8 * t, 128);
       ptx::mbar_init(bar_o_full + 8 * t, 1);
       ptx::mbar_init(bar_o_empty + 8 * t, 128);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       ptx::mbar_init(bar_kv_full + 8 * s, 1);
       ptx::mbar_init(bar_kv_empty + 8 * s, 1);
     }
@@ -254,24 +250,36 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
+    // The K/V ring holds kSlots slots of two tiles. Each slot is filled and
+    // released as a unit (one full and one empty barrier phase): per key tile
+    // j the MMA thread needs V_j and K_{j+1} together, so one wait covers both.
     const uint64_t pol_kv = ptx::policy_evict_last();
     const uint64_t pol_q = ptx::policy_evict_first();
-    uint32_t kv_it = 0, act = 0;
+    uint32_t slot_it = 0, act = 0;
     int load_idx = 0;
     bool ok = true;
-    auto load_kv = [&](const CUtensorMap* map, int j, int kvh, int b) -> bool {
-      const uint32_t st = kv_it % kStages;
-      const uint32_t ph = ((kv_it / kStages) & 1u) ^ 1u;
-      if (!bar_wait(bar_kv_empty + 8 * st, ph, abort_flag, p)) return false;
+    // Fill the next slot: tile (map0, key tile j0) at position 0 and, when
+    // map1 is given, (map1, j1) at position 1.
+    auto load_slot = [&](const CUtensorMap* map0, int j0, const CUtensorMap* map1, int j1, int kvh,
+                         int b) -> bool {
+      const uint32_t sl = slot_it % kSlots;
+      const uint32_t ph = ((slot_it / kSlots) & 1u) ^ 1u;
+      if (!bar_wait(bar_kv_empty + 8 * sl, ph, abort_flag, p)) return false;
       if (lane == 0 && load_idx != p.inject_skip_load) {
-        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * st, L::kTileBytes);
+        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * sl, (map1 ? 2 : 1) * L::kTileBytes);
+        const uint32_t dst = sKV + sl * 2 * L::kTileBytes;
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_4d(sKV + st * L::kTileBytes + c * L::kChunkBytes, map, bar_kv_full + 8 * st, c * 64, kvh,
-                           j * kBN, b, pol_kv);
+          ptx::tma_load_4d(dst + c * L::kChunkBytes, map0, bar_kv_full + 8 * sl, c * 64, kvh, j0 * kBN, b, pol_kv);
+        if (map1) {
+#pragma unroll
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_4d(dst + L::kTileBytes + c * L::kChunkBytes, map1, bar_kv_full + 8 * sl, c * 64, kvh,
+                             j1 * kBN, b, pol_kv);
+        }
       }
       __syncwarp();
-      ++kv_it;
+      ++slot_it;
       ++load_idx;
       return true;
     };
@@ -293,14 +301,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (idx >= p.n_items) continue;
       const WorkItem w = decode_item<KSPLIT>(p, idx);
       if (w.n_kv == 0) continue;
+      const int n = w.n_kv;
       // key-split: slot t runs key tiles t, t+2, ...; n1 of them for slot 1
-      const int n1 = w.n_kv / 2, n0 = w.n_kv - n1;
+      const int n1 = n / 2, n0 = n - n1;
+      // first slot: K_0 (and, key-split, K_1)
       if constexpr (KSPLIT)
-        ok = load_q(0, w.hq0, w.r0, w.b) && load_kv(&tm_k, 0, w.kvh, w.b) &&
-             (n1 == 0 || load_kv(&tm_k, 1, w.kvh, w.b));
+        ok = load_q(0, w.hq0, w.r0, w.b) && load_slot(&tm_k, 0, n1 > 0 ? &tm_k : nullptr, 1, w.kvh, w.b);
       else
-        ok = load_q(0, w.hq0, w.r0, w.b) && load_kv(&tm_k, 0, w.kvh, w.b) && load_q(1, w.hq1, w.r1, w.b) &&
-             load_kv(&tm_v, 0, w.kvh, w.b);
+        ok = load_q(0, w.hq0, w.r0, w.b) && load_slot(&tm_k, 0, nullptr, 0, w.kvh, w.b) &&
+             load_q(1, w.hq1, w.r1, w.b);
       // Q tiles are read once from HBM: pull the next item's into L2 now so
       // that its TMA load at the item boundary hits L2.
       if (ok && lane == 0) {
@@ -317,47 +326,47 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
       if constexpr (KSPLIT) {
-        // the MMA issuer's order: V(s, 0), K(s+1, 0), V(s, 1), K(s+1, 1)
-        for (int st = 0; ok && st < n0; ++st)
-          ok = load_kv(&tm_v, 2 * st, w.kvh, w.b) && (st + 1 >= n0 || load_kv(&tm_k, 2 * st + 2, w.kvh, w.b)) &&
-               (st >= n1 || load_kv(&tm_v, 2 * st + 1, w.kvh, w.b)) &&
-               (st + 1 >= n1 || load_kv(&tm_k, 2 * st + 3, w.kvh, w.b));
+        // per step s, for slot 0 then slot 1: (V of its tile, K of its next tile)
+        for (int st = 0; ok && st < n0; ++st) {
+          ok = load_slot(&tm_v, 2 * st, st + 1 < n0 ? &tm_k : nullptr, 2 * st + 2, w.kvh, w.b);
+          if (ok && st < n1) ok = load_slot(&tm_v, 2 * st + 1, st + 1 < n1 ? &tm_k : nullptr, 2 * st + 3, w.kvh, w.b);
+        }
       } else {
-        for (int j = 1; ok && j < w.n_kv; ++j)
-          ok = load_kv(&tm_k, j, w.kvh, w.b) && load_kv(&tm_v, j, w.kvh, w.b);
+        for (int j = 0; ok && j < n; ++j)
+          ok = load_slot(&tm_v, j, j + 1 < n ? &tm_k : nullptr, j + 1, w.kvh, w.b);
       }
       ++act;
     }
     if (!ok && lane == 0) {
       // Let copies already in flight land before the CTA leaves: wait (bounded)
-      // for the latest phase of every stage that was filled.
+      // for the latest phase of every slot that was filled.
       const uint64_t t0 = ptx::globaltimer_ns();
-      for (uint32_t k = (kv_it > (uint32_t)kStages ? kv_it - kStages : 0); k < kv_it; ++k) {
-        const uint32_t st = k % kStages, ph = (k / kStages) & 1u;
-        while (!ptx::mbar_try_wait(bar_kv_full + 8 * st, ph) && ptx::globaltimer_ns() - t0 < 2000000ull) {
+      for (uint32_t k = (slot_it > (uint32_t)kSlots ? slot_it - kSlots : 0); k < slot_it; ++k) {
+        const uint32_t sl = k % kSlots, ph = (k / kSlots) & 1u;
+        while (!ptx::mbar_try_wait(bar_kv_full + 8 * sl, ph) && ptx::globaltimer_ns() - t0 < 2000000ull) {
         }
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Pipe order per key tile j: P0 V_j (two halves), Q0 K_{j+1}^T, P1 V_j,
-    // Q1 K_{j+1}^T. The P V halves start as soon as the softmax has written
-    // the matching half of P.
+    // Pipe order per key tile j: P0 V_j, Q0 K_{j+1}^T, P1 V_j, Q1 K_{j+1}^T,
+    // each P_t V_j as soon as the softmax has written P_t. Ring tiles are
+    // numbered 2 * slot + position.
     constexpr uint32_t idesc_s = ptx::idesc_f16(BF16, kBM, kBN, false, false);
     constexpr uint32_t idesc_o = ptx::idesc_f16(BF16, kBM, D, false, true);
-    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // descriptor units per ring stage
+    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // descriptor units per ring tile
     // Descriptor bases; the start-address field (bits 0..13) is advanced by
     // adding byte offsets >> 4 (shared addresses stay below 256 KB).
     const uint64_t dq0 = ptx::sdesc_sw128(sQ, 16, 1024);
     const uint64_t dq1 = ptx::sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
     const uint64_t dk0 = ptx::sdesc_sw128(sKV, 16, 1024);                 // K: K-major
     const uint64_t dv0 = ptx::sdesc_sw128(sKV, L::kChunkBytes, 1024);     // V: MN-major
-    uint32_t kv_it = 0, act = 0, p_phase[2] = {0u, 0u};
+    uint32_t slot_it = 0, act = 0, p_phase[2] = {0u, 0u};
     bool ok = true;
-    // S_t = Q_t K^T: D/16 MMAs over the head dimension.
-    auto issue_s = [&](int t, uint32_t st) {
+    // S_t = Q_t K^T with K in ring tile kt: D/16 MMAs over the head dimension.
+    auto issue_s = [&](int t, uint32_t kt) {
       const uint64_t a = (t && !KSPLIT) ? dq1 : dq0;   // key-split: both slots read Q tile 0
-      const uint64_t bk = dk0 + st * kStageDesc;
+      const uint64_t bk = dk0 + kt * kStageDesc;
       const uint32_t d = tmem + (t ? kColS1 : kColS0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -365,9 +374,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::mma_ss(d, a + off, bk + off, idesc_s, ks > 0 ? 1u : 0u);
       }
     };
-    // O_t (+)= P_t V for keys [64 h, 64 h + 64): 4 MMAs, P from TMEM.
-    auto issue_pv = [&](int t, uint32_t st, int h, bool first) {
-      const uint64_t bv = dv0 + st * kStageDesc;
+    // O_t (+)= P_t V for keys [64 h, 64 h + 64) with V in ring tile vt: 4 MMAs,
+    // P from TMEM.
+    auto issue_pv = [&](int t, uint32_t vt, int h, bool first) {
+      const uint64_t bv = dv0 + vt * kStageDesc;
       const uint32_t d = tmem + (t ? kColO1 : kColO0);
       const uint32_t pa = tmem + (t ? kColS1 : kColS0);
 #pragma unroll
@@ -377,28 +387,23 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     (first && ks == 0) ? 0u : 1u);
       }
     };
-    auto wait_stage = [&](uint32_t it) -> bool {
-      return bar_wait(bar_kv_full + 8 * (it % kStages), (it / kStages) & 1u, abort_flag, p);
+    // Wait for the next slot; returns its index in `sl`.
+    auto wait_slot = [&](uint32_t& sl) -> bool {
+      sl = slot_it % kSlots;
+      const bool r = bar_wait(bar_kv_full + 8 * sl, (slot_it / kSlots) & 1u, abort_flag, p);
+      ++slot_it;
+      return r;
     };
-    // O_t (+)= P_t V for one key tile, each half of P as soon as the softmax
-    // has written it.
-    auto pv_tile = [&](int t, uint32_t v_stage, bool first) -> bool {
-      if (!bar_wait(bar_p_lo + 8 * t, p_phase[t], abort_flag, p)) return false;
-      if (ptx::mbar_test_wait(bar_p_hi + 8 * t, p_phase[t])) {
-        // all of P_t is written: one run of 8 P V MMAs
-        ptx::tc_fence_after();
-        if (lane == 0) {
-          issue_pv(t, v_stage, 0, first);
-          issue_pv(t, v_stage, 1, first);
-        }
-      } else {
-        // the softmax is still on keys 64..127: start on keys 0..63
-        ptx::tc_fence_after();
-        if (lane == 0) issue_pv(t, v_stage, 0, first);
-        __syncwarp();
-        if (!bar_wait(bar_p_hi + 8 * t, p_phase[t], abort_flag, p)) return false;
-        ptx::tc_fence_after();
-        if (lane == 0) issue_pv(t, v_stage, 1, first);
+    // O_t (+)= P_t V for one key tile, once the softmax has written all of P_t.
+    // (Waiting for each half separately costs the issuing thread one more
+    // barrier wait per tile, which the tensor pipe pays as idle time; P is
+    // normally complete long before the MMA thread gets to it.)
+    auto pv_tile = [&](int t, uint32_t vt, bool first) -> bool {
+      if (!bar_wait(bar_p_full + 8 * t, p_phase[t], abort_flag, p)) return false;
+      ptx::tc_fence_after();
+      if (lane == 0) {
+        issue_pv(t, vt, 0, first);
+        issue_pv(t, vt, 1, first);
       }
       p_phase[t] ^= 1u;
       return true;
@@ -409,59 +414,51 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (idx >= p.n_items) continue;
       const WorkItem w = decode_item<KSPLIT>(p, idx);
       if (w.n_kv == 0) continue;
+      const int n = w.n_kv;
       const uint32_t par = act & 1u;
+      uint32_t sl = 0;
       if constexpr (KSPLIT) {
         // Slot t runs key tiles t, t+2, ...: S_t from its first key tile, then
-        // per step P_t V and the next S_t, each slot on its own K/V stages.
-        const int n1 = w.n_kv / 2, n0 = w.n_kv - n1;
-        int s_left = w.n_kv;   // S MMAs of this item still to issue (each reads Q)
-        if (!(ok = bar_wait(bar_q_full, par, abort_flag, p))) break;
-        for (int t = 0; ok && t < 2; ++t) {
-          if (t == 1 && n1 == 0) {
-            // slot 1 has no key tile: close its O phase without an MMA
-            if (!(ok = bar_wait(bar_o_empty + 8, par ^ 1u, abort_flag, p))) break;
-            if (lane == 0) ptx::mma_commit(bar_o_full + 8);
-            __syncwarp();
-            break;
-          }
-          const uint32_t st = kv_it % kStages;
-          if (!(ok = wait_stage(kv_it))) break;
-          ++kv_it;
-          const bool last = --s_left == 0;
-          ptx::tc_fence_after();
-          if (lane == 0) {
-            issue_s(t, st);
-            ptx::mma_commit(bar_s_full + 8 * t);
-            ptx::mma_commit(bar_kv_empty + 8 * st);
-            if (last) ptx::mma_commit(bar_q_empty);
-          }
-          __syncwarp();
+        // per step P_t V and the next S_t, each from a ring slot of its own.
+        const int n1 = n / 2, n0 = n - n1;
+        // prologue: S_0 from K_0 (position 0) and S_1 from K_1 (position 1)
+        if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_slot(sl))) break;
+        if (n1 == 0) {
+          // slot 1 has no key tile: close its O phase without an MMA
+          if (!(ok = bar_wait(bar_o_empty + 8, par ^ 1u, abort_flag, p))) break;
         }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          issue_s(0, 2 * sl);
+          ptx::mma_commit(bar_s_full);
+          if (n1 > 0) {
+            issue_s(1, 2 * sl + 1);
+            ptx::mma_commit(bar_s_full + 8);
+          } else {
+            ptx::mma_commit(bar_o_full + 8);
+          }
+          ptx::mma_commit(bar_kv_empty + 8 * sl);
+          if (n0 == 1 && n1 <= 1) ptx::mma_commit(bar_q_empty);   // no S after these
+        }
+        __syncwarp();
         for (int sj = 0; ok && sj < n0; ++sj) {
           for (int t = 0; t < 2; ++t) {
             const int nt = t ? n1 : n0;
             if (sj >= nt) break;
-            const uint32_t v_stage = kv_it % kStages;
-            if (!(ok = wait_stage(kv_it))) break;
-            ++kv_it;
+            if (!(ok = wait_slot(sl))) break;
             if (sj == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-            if (!(ok = pv_tile(t, v_stage, sj == 0))) break;
-            if (lane == 0) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
-            __syncwarp();
-            if (sj + 1 < nt) {
-              const uint32_t k_stage = kv_it % kStages;
-              if (!(ok = wait_stage(kv_it))) break;
-              ++kv_it;
-              const bool last = --s_left == 0;
-              ptx::tc_fence_after();
-              if (lane == 0) {
-                issue_s(t, k_stage);
+            if (!(ok = pv_tile(t, 2 * sl, sj == 0))) break;
+            if (lane == 0) {
+              if (sj + 1 < nt) {
+                issue_s(t, 2 * sl + 1);
                 ptx::mma_commit(bar_s_full + 8 * t);
-                ptx::mma_commit(bar_kv_empty + 8 * k_stage);
-                if (last) ptx::mma_commit(bar_q_empty);
+                // Q's last reader: slot 1's last S when slot 1 runs as many
+                // steps as slot 0, else slot 0's
+                if (sj + 2 == n0 && (t == 1 || n1 < n0)) ptx::mma_commit(bar_q_empty);
+              } else {
+                ptx::mma_commit(bar_o_full + 8 * t);
               }
-            } else if (lane == 0) {
-              ptx::mma_commit(bar_o_full + 8 * t);
+              ptx::mma_commit(bar_kv_empty + 8 * sl);
             }
             __syncwarp();
           }
@@ -469,53 +466,42 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ++act;
         continue;
       }
-      uint32_t k_stage = kv_it % kStages;
       // prologue: S_0 = Q_0 K_0^T as soon as Q_0 and K_0 land, then S_1
-      if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_stage(kv_it))) break;
+      if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_slot(sl))) break;
       ptx::tc_fence_after();
       if (lane == 0) {
-        issue_s(0, k_stage);
+        issue_s(0, 2 * sl);
         ptx::mma_commit(bar_s_full);
-        if (w.n_kv == 1) ptx::mma_commit(bar_q_empty);
+        if (n == 1) ptx::mma_commit(bar_q_empty);
       }
       __syncwarp();
       if (!(ok = bar_wait(bar_q_full + 8, par, abort_flag, p))) break;
       ptx::tc_fence_after();
       if (lane == 0) {
-        issue_s(1, k_stage);
+        issue_s(1, 2 * sl);
         ptx::mma_commit(bar_s_full + 8);
-        ptx::mma_commit(bar_kv_empty + 8 * k_stage);
-        if (w.n_kv == 1) ptx::mma_commit(bar_q_empty + 8);
+        ptx::mma_commit(bar_kv_empty + 8 * sl);
+        if (n == 1) ptx::mma_commit(bar_q_empty + 8);
       }
       __syncwarp();
-      ++kv_it;
-      for (int j = 0; ok && j < w.n_kv; ++j) {
-        const bool more = (j + 1 < w.n_kv);
-        const bool last_s = (j + 2 == w.n_kv);   // S_t(j+1) is the item's last use of Q_t
-        const uint32_t v_stage = kv_it % kStages;
-        // V_j and (when there is one) K_{j+1} are normally resident long before
-        // they are needed; wait for both here so that each tile's P V and next
-        // Q K^T go out as one uninterrupted run of MMAs.
-        if (!(ok = wait_stage(kv_it))) break;
-        ++kv_it;
-        if (more) {
-          if (!(ok = wait_stage(kv_it))) break;
-          k_stage = kv_it % kStages;
-          ++kv_it;
-        }
+      for (int j = 0; ok && j < n; ++j) {
+        const bool more = (j + 1 < n);
+        const bool last_s = (j + 2 == n);   // S_t(j+1) is the item's last use of Q_t
+        // one slot holds V_j (position 0) and K_{j+1} (position 1), so each
+        // tile's P V and next Q K^T go out as one run of MMAs after one wait
+        if (!(ok = wait_slot(sl))) break;
         for (int t = 0; t < 2; ++t) {
           if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-          if (!(ok = pv_tile(t, v_stage, j == 0))) break;
+          if (!(ok = pv_tile(t, 2 * sl, j == 0))) break;
           if (lane == 0) {
-            if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * v_stage);
             if (more) {
-              issue_s(t, k_stage);
+              issue_s(t, 2 * sl + 1);
               ptx::mma_commit(bar_s_full + 8 * t);
-              if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * k_stage);
               if (last_s) ptx::mma_commit(bar_q_empty + 8 * t);
             } else {
               ptx::mma_commit(bar_o_full + 8 * t);
             }
+            if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * sl);
           }
           __syncwarp();
         }
@@ -672,9 +658,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::tmem_st_32x32b_x32(tO + c * 32, orr);
           }
         }
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_p_lo + 8 * t);
         {
           uint32_t pk[32];
           exp_half(1, pk);
@@ -687,7 +670,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_p_hi + 8 * t);
+        ptx::mbar_arrive(bar_p_full + 8 * t);
       }
       if (!ok) break;
       if constexpr (KSPLIT) {
