@@ -480,16 +480,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (lane == 0) {
         issue_s(1, 2 * sl);
         ptx::mma_commit(bar_s_full + 8);
-        ptx::mma_commit(bar_kv_empty + 8 * sl);
         if (n == 1) ptx::mma_commit(bar_q_empty + 8);
       }
       __syncwarp();
       for (int j = 0; ok && j < n; ++j) {
         const bool more = (j + 1 < n);
         const bool last_s = (j + 2 == n);   // S_t(j+1) is the item's last use of Q_t
-        // one slot holds V_j (position 0) and K_{j+1} (position 1), so each
-        // tile's P V and next Q K^T go out as one run of MMAs after one wait
-        if (!(ok = wait_slot(sl))) break;
+        // One slot holds V_j (position 0) and K_{j+1} (position 1). The MMA
+        // thread does not wait for it: the tile-0 softmax checks it before it
+        // signals P_0(j), so P_0 ready implies the slot is full, and the
+        // tile-1 softmax releases it. Each barrier wait or commit the MMA
+        // thread skips is time the tensor pipe would otherwise sit idle.
+        sl = slot_it % kSlots;
+        ++slot_it;
         for (int t = 0; t < 2; ++t) {
           if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
           if (!(ok = pv_tile(t, 2 * sl, j == 0))) break;
@@ -501,7 +504,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             } else {
               ptx::mma_commit(bar_o_full + 8 * t);
             }
-            if (t == 1) ptx::mma_commit(bar_kv_empty + 8 * sl);
           }
           __syncwarp();
         }
@@ -526,6 +528,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float sl2 = p.scale_log2;
     const int offset = p.Sk - p.Sq;
     uint32_t s_phase = 0, act = 0;
+    // Row-tile pairs: K/V ring slot uses, counted like the producer's (an
+    // item of n key tiles uses n + 1 slots: K_0, then (V_j, K_{j+1})).
+    uint32_t slot_it = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int idx = item_of_round(round, cta, grid);
@@ -564,11 +569,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       float m_ref = -__int_as_float(0x7f800000);
       float l_exact = 0.0f, l_corr = 0.0f;
+      const uint32_t use0 = slot_it;   // row-tile pairs: this item's first ring slot use
       // key-split: this slot's key tiles are t, t+2, ...
       const int n_mine = KSPLIT ? (t ? w.n_kv / 2 : w.n_kv - w.n_kv / 2) : w.n_kv;
       for (int sj = 0; sj < n_mine; ++sj) {
         const int j = KSPLIT ? 2 * sj + t : sj;   // key tile
         if (!(ok = bar_wait(bar_s_full + 8 * t, s_phase, abort_flag, p))) break;
+        if constexpr (!KSPLIT) {
+          // S_1(j) has completed, and with it every MMA that reads ring slot
+          // use j (K_0 when j = 0, else V_{j-1} and K_j): release the slot
+          if (warp == 4 && lane == 0) ptx::mbar_arrive(bar_kv_empty + 8 * ((use0 + j) % kSlots));
+          // The MMA thread reads V_j and K_{j+1} (slot use j + 1) as soon as
+          // it sees P_0(j), without a wait of its own: P_0(j) is signalled
+          // only after this wait (normally long satisfied) has seen the slot
+          // full.
+          if (warp == 0) {
+            const uint32_t u = use0 + j + 1;
+            bool r = true;
+            if (lane == 0) r = bar_wait(bar_kv_full + 8 * (u % kSlots), (u / kSlots) & 1u, abort_flag, p);
+            if (!(ok = __shfl_sync(0xffffffffu, r, 0))) break;
+          }
+        }
         s_phase ^= 1u;
         ptx::tc_fence_after();
         uint32_t sr[128];
@@ -752,6 +773,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       // ---- epilogue: O = O~ / l, LSE = (m + log2 l) * ln 2
       if (!(ok = bar_wait(bar_o_full + 8 * t, act & 1u, abort_flag, p))) break;
+      // P_1 V_{n-1}, the last reader of slot use n, has completed: release it
+      if (t == 1 && warp == 4 && lane == 0) ptx::mbar_arrive(bar_kv_empty + 8 * ((use0 + w.n_kv) % kSlots));
+      slot_it = use0 + w.n_kv + 1;
       ptx::tc_fence_after();
       uint32_t orr[D];
       if constexpr (D == 128) {
