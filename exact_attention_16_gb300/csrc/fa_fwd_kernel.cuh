@@ -351,10 +351,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // ------------------------------------------------------------ MMA issuer
     // Pipe order per key tile j: P0 V_j, Q0 K_{j+1}^T, P1 V_j, Q1 K_{j+1}^T,
     // each P_t V_j as soon as the softmax has written P_t. Ring tiles are
-    // numbered 2 * slot + position.
+    // numbered 2 * slot + position. Lane 0 alone runs the loop.
+    //
+    // On sm_103a the tensor pipe holds only a few queued MMAs, so every cycle
+    // this thread spends outside tcgen05.mma issue can leave it idle. Measured
+    // in isolation: a commit costs nothing, a satisfied mbarrier.test_wait 17
+    // cycles, but a test_wait right behind a commit about 60. So the readiness
+    // of the next P is tested between the MMAs of a group, not after its
+    // commit, and the result is used when that group's turn comes.
     constexpr uint32_t idesc_s = ptx::idesc_f16(BF16, kBM, kBN, false, false);
     constexpr uint32_t idesc_o = ptx::idesc_f16(BF16, kBM, D, false, true);
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // descriptor units per ring tile
+    constexpr int kS = D / 16;    // MMAs per S tile (over the head dimension)
+    constexpr int kPV = kBN / 16; // MMAs per P V (over the keys)
     // Descriptor bases; the start-address field (bits 0..13) is advanced by
     // adding byte offsets >> 4 (shared addresses stay below 256 KB).
     const uint64_t dq0 = ptx::sdesc_sw128(sQ, 16, 1024);
@@ -363,26 +372,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint64_t dv0 = ptx::sdesc_sw128(sKV, L::kChunkBytes, 1024);     // V: MN-major
     uint32_t slot_it = 0, act = 0, p_phase[2] = {0u, 0u};
     bool ok = true;
-    // S_t = Q_t K^T with K in ring tile kt: D/16 MMAs over the head dimension.
-    auto issue_s = [&](int t, uint32_t kt) {
+    // S_t = Q_t K^T with K in ring tile kt, k-steps [k0, k1).
+    auto issue_s = [&](int t, uint32_t kt, int k0, int k1) {
       const uint64_t a = (t && !KSPLIT) ? dq1 : dq0;   // key-split: both slots read Q tile 0
       const uint64_t bk = dk0 + kt * kStageDesc;
       const uint32_t d = tmem + (t ? kColS1 : kColS0);
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
+      for (int ks = 0; ks < kS; ++ks) {
+        if (ks < k0 || ks >= k1) continue;
         const uint32_t off = static_cast<uint32_t>(((ks / 4) * L::kChunkBytes + (ks % 4) * 32) >> 4);
         ptx::mma_ss(d, a + off, bk + off, idesc_s, ks > 0 ? 1u : 0u);
       }
     };
-    // O_t (+)= P_t V for keys [64 h, 64 h + 64) with V in ring tile vt: 4 MMAs,
+    // O_t (+)= P_t V with V in ring tile vt, k-steps (16 keys each) [k0, k1);
     // P from TMEM.
-    auto issue_pv = [&](int t, uint32_t vt, int h, bool first) {
+    auto issue_pv = [&](int t, uint32_t vt, int k0, int k1, bool first) {
       const uint64_t bv = dv0 + vt * kStageDesc;
       const uint32_t d = tmem + (t ? kColO1 : kColO0);
       const uint32_t pa = tmem + (t ? kColS1 : kColS0);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int ks = 4 * h + k;
+      for (int ks = 0; ks < kPV; ++ks) {
+        if (ks < k0 || ks >= k1) continue;
         ptx::mma_ts(d, pa + ks * 8, bv + static_cast<uint32_t>((ks * 16 * 128) >> 4), idesc_o,
                     (first && ks == 0) ? 0u : 1u);
       }
@@ -394,63 +404,56 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ++slot_it;
       return r;
     };
-    // O_t (+)= P_t V for one key tile, once the softmax has written all of P_t.
-    // (Waiting for each half separately costs the issuing thread one more
-    // barrier wait per tile, which the tensor pipe pays as idle time; P is
-    // normally complete long before the MMA thread gets to it.)
-    auto pv_tile = [&](int t, uint32_t vt, bool first) -> bool {
-      if (!bar_wait(bar_p_full + 8 * t, p_phase[t], abort_flag, p)) return false;
-      ptx::tc_fence_after();
-      if (lane == 0) {
-        issue_pv(t, vt, 0, first);
-        issue_pv(t, vt, 1, first);
-      }
+    // P_t ready (all of it: one wait per tile, not one per half). `seen` says
+    // an earlier test_wait already saw this phase complete.
+    auto wait_p = [&](int t, bool seen) -> bool {
+      if (!seen && !bar_wait(bar_p_full + 8 * t, p_phase[t], abort_flag, p)) return false;
       p_phase[t] ^= 1u;
+      ptx::tc_fence_after();
       return true;
     };
-    for (int round = 0; ok; ++round) {
-      const int idx = item_of_round(round, cta, grid);
-      if (round * grid >= p.n_items) break;
-      if (idx >= p.n_items) continue;
-      const WorkItem w = decode_item<KSPLIT>(p, idx);
-      if (w.n_kv == 0) continue;
-      const int n = w.n_kv;
-      const uint32_t par = act & 1u;
-      uint32_t sl = 0;
-      if constexpr (KSPLIT) {
-        // Slot t runs key tiles t, t+2, ...: S_t from its first key tile, then
-        // per step P_t V and the next S_t, each from a ring slot of its own.
-        const int n1 = n / 2, n0 = n - n1;
-        // prologue: S_0 from K_0 (position 0) and S_1 from K_1 (position 1)
-        if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_slot(sl))) break;
-        if (n1 == 0) {
-          // slot 1 has no key tile: close its O phase without an MMA
-          if (!(ok = bar_wait(bar_o_empty + 8, par ^ 1u, abort_flag, p))) break;
-        }
-        ptx::tc_fence_after();
-        if (lane == 0) {
-          issue_s(0, 2 * sl);
+    if (lane == 0) {
+      for (int round = 0; ok; ++round) {
+        const int idx = item_of_round(round, cta, grid);
+        if (round * grid >= p.n_items) break;
+        if (idx >= p.n_items) continue;
+        const WorkItem w = decode_item<KSPLIT>(p, idx);
+        if (w.n_kv == 0) continue;
+        const int n = w.n_kv;
+        const uint32_t par = act & 1u;
+        uint32_t sl = 0;
+        if constexpr (KSPLIT) {
+          // Slot t runs key tiles t, t+2, ...: S_t from its first key tile,
+          // then per step P_t V and the next S_t, each from a ring slot of its
+          // own.
+          const int n1 = n / 2, n0 = n - n1;
+          // prologue: S_0 from K_0 (position 0) and S_1 from K_1 (position 1)
+          if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_slot(sl))) break;
+          if (n1 == 0) {
+            // slot 1 has no key tile: close its O phase without an MMA
+            if (!(ok = bar_wait(bar_o_empty + 8, par ^ 1u, abort_flag, p))) break;
+          }
+          ptx::tc_fence_after();
+          issue_s(0, 2 * sl, 0, kS);
           ptx::mma_commit(bar_s_full);
           if (n1 > 0) {
-            issue_s(1, 2 * sl + 1);
+            issue_s(1, 2 * sl + 1, 0, kS);
             ptx::mma_commit(bar_s_full + 8);
           } else {
             ptx::mma_commit(bar_o_full + 8);
           }
           ptx::mma_commit(bar_kv_empty + 8 * sl);
           if (n0 == 1 && n1 <= 1) ptx::mma_commit(bar_q_empty);   // no S after these
-        }
-        __syncwarp();
-        for (int sj = 0; ok && sj < n0; ++sj) {
-          for (int t = 0; t < 2; ++t) {
-            const int nt = t ? n1 : n0;
-            if (sj >= nt) break;
-            if (!(ok = wait_slot(sl))) break;
-            if (sj == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-            if (!(ok = pv_tile(t, 2 * sl, sj == 0))) break;
-            if (lane == 0) {
+          for (int sj = 0; ok && sj < n0; ++sj) {
+            for (int t = 0; t < 2; ++t) {
+              const int nt = t ? n1 : n0;
+              if (sj >= nt) break;
+              if (!(ok = wait_slot(sl))) break;
+              if (sj == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
+              if (!(ok = wait_p(t, false))) break;
+              issue_pv(t, 2 * sl, 0, kPV, sj == 0);
               if (sj + 1 < nt) {
-                issue_s(t, 2 * sl + 1);
+                issue_s(t, 2 * sl + 1, 0, kS);
                 ptx::mma_commit(bar_s_full + 8 * t);
                 // Q's last reader: slot 1's last S when slot 1 runs as many
                 // steps as slot 0, else slot 0's
@@ -460,64 +463,63 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               }
               ptx::mma_commit(bar_kv_empty + 8 * sl);
             }
-            __syncwarp();
           }
+          ++act;
+          continue;
         }
-        ++act;
-        continue;
-      }
-      // prologue: S_0 = Q_0 K_0^T as soon as Q_0 and K_0 land, then S_1
-      if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_slot(sl))) break;
-      ptx::tc_fence_after();
-      if (lane == 0) {
-        issue_s(0, 2 * sl);
+        // prologue: S_0 = Q_0 K_0^T as soon as Q_0 and K_0 land, then S_1
+        if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_slot(sl))) break;
+        ptx::tc_fence_after();
+        issue_s(0, 2 * sl, 0, kS);
         ptx::mma_commit(bar_s_full);
         if (n == 1) ptx::mma_commit(bar_q_empty);
-      }
-      __syncwarp();
-      if (!(ok = bar_wait(bar_q_full + 8, par, abort_flag, p))) break;
-      ptx::tc_fence_after();
-      if (lane == 0) {
-        issue_s(1, 2 * sl);
+        if (!(ok = bar_wait(bar_q_full + 8, par, abort_flag, p))) break;
+        ptx::tc_fence_after();
+        issue_s(1, 2 * sl, 0, kS);
         ptx::mma_commit(bar_s_full + 8);
         if (n == 1) ptx::mma_commit(bar_q_empty + 8);
-      }
-      __syncwarp();
-      for (int j = 0; ok && j < n; ++j) {
-        const bool more = (j + 1 < n);
-        const bool last_s = (j + 2 == n);   // S_t(j+1) is the item's last use of Q_t
-        // One slot holds V_j (position 0) and K_{j+1} (position 1). The MMA
-        // thread does not wait for it: the tile-0 softmax checks it before it
-        // signals P_0(j), so P_0 ready implies the slot is full, and the
-        // tile-1 softmax releases it. Each barrier wait or commit the MMA
-        // thread skips is time the tensor pipe would otherwise sit idle.
-        sl = slot_it % kSlots;
-        ++slot_it;
-        for (int t = 0; t < 2; ++t) {
-          if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-          if (!(ok = pv_tile(t, 2 * sl, j == 0))) break;
-          if (lane == 0) {
+        bool seen[2] = {false, false};   // P_t's next phase already seen complete
+        for (int j = 0; ok && j < n; ++j) {
+          const bool more = (j + 1 < n);
+          const bool last_s = (j + 2 == n);   // S_t(j+1) is the item's last use of Q_t
+          // One slot holds V_j (position 0) and K_{j+1} (position 1). The MMA
+          // thread does not wait for it: the tile-0 softmax checks it before
+          // it signals P_0(j), so P_0 ready implies the slot is full, and the
+          // tile-1 softmax releases it.
+          sl = slot_it % kSlots;
+          ++slot_it;
+          for (int t = 0; t < 2; ++t) {
+            if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
+            if (!(ok = wait_p(t, seen[t]))) break;
+            // the group: P_t V_j, then Q_t K_{j+1}^T; the next group's P is
+            // tested just before the group's last MMA
+            const int o = 1 - t;
             if (more) {
-              issue_s(t, 2 * sl + 1);
+              issue_pv(t, 2 * sl, 0, kPV, j == 0);
+              issue_s(t, 2 * sl + 1, 0, kS - 1);
+              seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
+              issue_s(t, 2 * sl + 1, kS - 1, kS);
               ptx::mma_commit(bar_s_full + 8 * t);
               if (last_s) ptx::mma_commit(bar_q_empty + 8 * t);
             } else {
+              issue_pv(t, 2 * sl, 0, kPV - 1, j == 0);
+              seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
+              issue_pv(t, 2 * sl, kPV - 1, kPV, false);
               ptx::mma_commit(bar_o_full + 8 * t);
             }
           }
-          __syncwarp();
+        }
+        ++act;
+      }
+      if (!ok) {
+        // Wait (bounded) for every MMA already issued before TMEM is released.
+        ptx::mma_commit(bar_teardown);
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar_teardown, 0) && ptx::globaltimer_ns() - t0 < 2000000ull) {
         }
       }
-      ++act;
     }
-    if (!ok) {
-      // Wait (bounded) for every MMA already issued before TMEM is released.
-      if (lane == 0) ptx::mma_commit(bar_teardown);
-      __syncwarp();
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(bar_teardown, 0) && ptx::globaltimer_ns() - t0 < 2000000ull) {
-      }
-    }
+    __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
     const int t = warp >> 2;                 // query tile of this warpgroup
