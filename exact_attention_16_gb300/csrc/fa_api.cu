@@ -155,14 +155,16 @@ void set_items(fa::FwdParams& p, bool ksplit) {
 
 // Finishing time of the busiest CTA under the static serpentine schedule, in
 // key-tile steps (one step = one key tile for both slots of a CTA). A key-split
-// item of n key tiles takes ceil(n / 2) steps, which cost as much as row-tile-
-// pair steps; every item also pays 2.25 steps of Q load, pipeline fill and
-// epilogue. Both constants are fitted to GB300 timings of 18 shapes (MHA and
-// GQA, causal and not, 0.5K to 32K keys), on which the model picks the faster
-// schedule every time and predicts the time ratio within 8 %.
+// item of n key tiles takes ceil(n / 2) steps, each 1.125 times as long as a
+// row-tile-pair step (every K/V tile feeds one slot instead of two, and the
+// MMA thread waits for each slot's K/V itself); every item also pays 1.25
+// steps of Q load, pipeline fill and epilogue. Both constants are fitted to
+// GB300 timings of 18 shapes (MHA and GQA, causal and not, 0.5K to 32K keys),
+// on which the model picks the faster schedule every time and predicts the
+// time ratio within 9 %.
 double schedule_makespan(const fa::FwdParams& p, bool ksplit, int grid) {
-  constexpr double kItemOverhead = 2.25;
-  constexpr double kSplitStep = 1.0;
+  constexpr double kItemOverhead = 1.25;
+  constexpr double kSplitStep = 1.125;
   const int n_items = p.n_items;
   double worst = 0.0;
   for (int cta = 0; cta < grid; ++cta) {

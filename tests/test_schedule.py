@@ -74,17 +74,18 @@ def test_invalid_sizes_rejected(args):
 # (B, Sq, Sk, Hq, Hkv, causal) -> the faster schedule measured on a GB300
 # (CUDA-graph timings of both forced schedules, microseconds pairs / split)
 MEASURED = [
-    ((1, 1280, 1536, 16, 16, 1), 1),   # 22.9 / 14.7
-    ((1, 2048, 2048, 8, 8, 1), 1),     # 30.9 / 18.7
-    ((1, 4096, 4096, 8, 8, 1), 1),     # 52.5 / 29.8
-    ((1, 512, 4096, 32, 8, 1), 1),     # 52.0 / 29.5
-    ((1, 128, 32768, 8, 8, 0), 1),     # 375.7 / 198.8
-    ((1, 3072, 3072, 16, 16, 1), 1),   # 41.0 / 37.4
-    ((1, 16384, 16384, 4, 4, 1), 1),   # 193.1 / 189.1
-    ((1, 1536, 1536, 16, 16, 0), 0),   # 23.2 / 26.4
-    ((4, 512, 512, 32, 32, 0), 0),     # 19.4 / 25.7
-    ((1, 4096, 4096, 16, 4, 1), 0),    # 52.5 / 56.1
-    ((2, 1024, 1024, 32, 8, 1), 0),    # 20.0 / 27.8
+    ((1, 1280, 1536, 16, 16, 1), 1),   # 22.7 / 14.8
+    ((1, 2048, 2048, 8, 8, 1), 1),     # 29.6 / 19.1
+    ((1, 4096, 4096, 8, 8, 1), 1),     # 50.5 / 29.6
+    ((1, 512, 4096, 32, 8, 1), 1),     # 50.1 / 29.3
+    ((1, 128, 32768, 8, 8, 0), 1),     # 367.0 / 199.5
+    ((1, 3072, 3072, 16, 16, 1), 1),   # 40.3 / 38.0
+    ((1, 16384, 16384, 4, 4, 1), 0),   # 183.4 / 188.7
+    ((1, 8192, 8192, 8, 1, 1), 0),     # 94.4 / 96.8
+    ((1, 1536, 1536, 16, 16, 0), 0),   # 23.9 / 26.6
+    ((4, 512, 512, 32, 32, 0), 0),     # 19.5 / 25.8
+    ((1, 4096, 4096, 16, 4, 1), 0),    # 50.7 / 55.7
+    ((2, 1024, 1024, 32, 8, 1), 0),    # 20.5 / 27.9
 ]
 
 
