@@ -12,6 +12,8 @@ from .api import (  # noqa: F401
     fa_debug_set_schedule,
     fa_fwd,
     fa_fwd_strided,
+    fa_fwd_host,
+    fa_fwd_host_workspace_size,
     fa_merge,
     fa_fwd_decode,
     fa_decode_workspace_size,

@@ -24,6 +24,8 @@ __all__ = [
     "fa_fwd_decode",
     "fa_decode_workspace_size",
     "fa_fwd_decode_noalloc",
+    "fa_fwd_host",
+    "fa_fwd_host_workspace_size",
     "fa_status",
     "fa_status_string",
     "fa_version",
@@ -71,6 +73,10 @@ EXPORTED_SYMBOLS = {
     "fa_version": (ctypes.c_int, []),
     "fa_debug_set_fault": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "fa_debug_set_schedule": (ctypes.c_int, [ctypes.c_int]),
+    "fa_fwd_host_workspace_size": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6
+                    + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_ulonglong,
+                       ctypes.c_void_p]),
     "fa_fwd_schedule": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)]),
 }
 
@@ -306,6 +312,73 @@ def fa_fwd_decode_noalloc(q, k, v, *, scale=None, causal=False, num_splits=0, ou
                                          _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_decode_noalloc")
+    return out, lse
+
+
+def fa_fwd_host_workspace_size(B, Sq, Sk, Hq, Hkv, D) -> int:
+    """Device bytes fa_fwd_host needs (a device copy of q, k, v, O and LSE)."""
+    out = ctypes.c_ulonglong(0)
+    rc = lib().fa_fwd_host_workspace_size(B, Sq, Sk, Hq, Hkv, D, ctypes.byref(out))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_host_workspace_size")
+    return int(out.value)
+
+
+def fa_fwd_host(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=True, workspace=None,
+                device=None, stream=None, synchronize=True):
+    """Attention on tensors in host memory: copies in, kernel and copies out
+    pipelined per chunk of batches or KV heads (include/fa.h, fa_fwd_host).
+
+    q: (B, Sq, Hq, D); k, v: (B, Sk, Hkv, D) contiguous CPU tensors of one
+    16-bit dtype (page-locked memory lets the copies overlap the kernels).
+    ``out``/``lse`` are CPU tensors to fill (allocated page-locked when
+    omitted). ``workspace`` is a CUDA uint8 tensor of at least
+    fa_fwd_host_workspace_size(...) bytes (allocated for this call when
+    omitted). With ``synchronize`` the call returns once the results are in
+    ``out``/``lse``; otherwise the caller synchronises ``stream`` first.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CPU tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError("k and v must be (B, Sk, Hkv, D) matching q")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    elif tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype or out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU tensor shaped and typed like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, pin_memory=True)
+    elif lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32 or lse.is_cuda
+                              or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 (B, Hq, Sq) CPU tensor")
+    dev = torch.cuda.current_device() if device is None else torch.device(device).index
+    need = fa_fwd_host_workspace_size(B, Sq, Sk, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=torch.device("cuda", dev))
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+
+    def call():
+        h = _stream_handle(stream, dev)
+        rc = lib().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, B, Sq, Sk, Hq, Hkv, D, float(scale),
+                               int(bool(causal)), code, workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), h)
+        if rc != FA_OK:
+            raise FAError(rc, "fa_fwd_host")
+        if synchronize:
+            (stream if stream is not None else torch.cuda.current_stream(dev)).synchronize()
+
+    _call_on(dev, call)
     return out, lse
 
 

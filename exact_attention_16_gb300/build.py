@@ -28,7 +28,7 @@ NVCC_FLAGS = [
 ]
 
 TARGETS = {
-    "libfa_gb300.so": ["fa_api.cu", "fa_merge.cu", "fa_decode.cu", "fa_decode_noalloc.cu"],
+    "libfa_gb300.so": ["fa_api.cu", "fa_merge.cu", "fa_decode.cu", "fa_decode_noalloc.cu", "fa_host.cu"],
     "libfa_probes.so": ["probes.cu"],
 }
 

@@ -172,6 +172,43 @@ int fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, 
                           fa_stream_t stream);
 
 /*
+ * fa_fwd_host_workspace_size — device bytes fa_fwd_host needs for these
+ * sizes: room for a device copy of Q, K, V, O and LSE (each 256-byte
+ * aligned). FA_ERR_INVALID_ARG for a null `bytes` or a negative size.
+ */
+int fa_fwd_host_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D, unsigned long long* bytes);
+
+/*
+ * fa_fwd_host — fa_fwd for tensors in HOST memory. The operation, layouts
+ * (contiguous (B, S, H, D) q, k, v, o; contiguous (B, Hq, Sq) fp32 lse, which
+ * may be NULL), dtypes, masks and results are those of fa_fwd; only the
+ * placement differs: q, k, v, o, lse are host pointers (page-locked memory
+ * lets the copies run asynchronously and overlap; pageable memory works but
+ * serialises them). `workspace` is a device buffer of at least
+ * fa_fwd_host_workspace_size(...) bytes, 256-byte aligned, owned by the
+ * caller and not read before being written.
+ *
+ * The call splits the problem into up to four chunks (ranges of batches, or
+ * when B = 1 ranges of KV heads with their query heads; at most one chunk
+ * per 48 MiB of copies, so small problems run as one) and pipelines, per
+ * chunk, the host-to-device copy of its Q, K, V, the attention kernel and the
+ * device-to-host copy of its O and LSE: copies run on two streams of the
+ * library (one per direction, created once per device), kernels on `stream`,
+ * ordered by events. It returns after enqueueing; o and lse are complete
+ * once `stream` has completed (the call makes `stream` wait for the last
+ * copy). Overlapping calls on one device share the library's copy streams
+ * and so run one after another; they must not share a workspace.
+ *
+ * Errors: those of fa_fwd for the arguments it shares, FA_ERR_INVALID_ARG for
+ * a null, misaligned or too small workspace, FA_ERR_CUDA when a copy, event
+ * or stream call fails. "NVIDIA闪存注意力实操" and the other pages describe
+ * the kernel only; this call is the data movement around it.
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk, int Hq,
+                int Hkv, int D, float scale, int causal, int dtype, void* workspace,
+                unsigned long long workspace_bytes, fa_stream_t stream);
+
+/*
  * fa_status — synchronise `stream`, then read and clear the device status
  * word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's bounded
  * wait on an mbarrier ran out (the kernel then released its tensor memory

@@ -175,3 +175,35 @@ def test_decode_rejects_before_any_launch(lib):
     assert c(scale=0.0) == api.FA_ERR_INVALID_ARG
     assert c(Hq=258, Hkv=2) == api.FA_ERR_UNSUPPORTED
     assert c(B=0) == api.FA_OK
+
+
+def test_host_workspace_size_formula(lib):
+    # device copy of q, k, v, o (16-bit) and lse (fp32), each rounded up to 256 bytes
+    B, Sq, Sk, Hq, Hkv, D = 2, 300, 257, 8, 2, 128
+    up = lambda x: (x + 255) // 256 * 256
+    q = B * Sq * Hq * D * 2
+    kv = B * Sk * Hkv * D * 2
+    want = up(q) + 2 * up(kv) + up(q) + up(B * Hq * Sq * 4)
+    assert api.fa_fwd_host_workspace_size(B, Sq, Sk, Hq, Hkv, D) == want
+    with pytest.raises(api.FAError):
+        api.fa_fwd_host_workspace_size(-1, Sq, Sk, Hq, Hkv, D)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), api.FA_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), api.FA_ERR_INVALID_ARG),
+    (dict(D=72), api.FA_ERR_UNSUPPORTED),
+    (dict(q=None), api.FA_ERR_INVALID_ARG),
+    (dict(workspace=None), api.FA_ERR_INVALID_ARG),
+    (dict(workspace_bytes=16), api.FA_ERR_INVALID_ARG),
+    (dict(workspace=256 + 16), api.FA_ERR_INVALID_ARG),      # not 256-byte aligned
+    (dict(B=0), api.FA_OK),
+])
+def test_host_entry_validates_before_any_copy(lib, kw, code):
+    args = dict(q=64, k=64, v=64, o=64, lse=None, B=1, Sq=4, Sk=4, Hq=2, Hkv=1, D=128, scale=0.125, causal=0,
+                dtype=1, workspace=256, workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    rc = lib.fa_fwd_host(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["Sq"], args["Sk"],
+                         args["Hq"], args["Hkv"], args["D"], args["scale"], args["causal"], args["dtype"],
+                         args["workspace"], args["workspace_bytes"], args["stream"])
+    assert rc == code
