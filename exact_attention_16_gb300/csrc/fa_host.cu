@@ -1,11 +1,14 @@
 // fa_fwd_host: the forward pass for tensors that live in host memory. The
 // caller gives host Q, K, V, O, LSE and one device workspace; the call splits
-// the problem into chunks (batch ranges, or ranges of KV heads with their
-// query heads) and pipelines, per chunk, the host-to-device copy of its Q, K
-// and V, the attention kernel on it, and the device-to-host copy of its O and
-// LSE, on two copy streams of the library's and the caller's stream, so that
-// copies in both directions overlap the kernels of other chunks. The device copy keeps the host layout; a chunk is
-// a strided view of it, computed by fa_fwd_strided.
+// the problem into chunks (batch ranges, or ranges of KV heads and query
+// rows) and pipelines, per chunk, the host-to-device copy of its Q and of the
+// K/V rows it newly needs, the attention kernel on it, and the device-to-host
+// copy of its O and LSE. Copies run on two streams of the library (one per
+// direction), kernels on the caller's stream and one more library stream in
+// turn, so that copies in both directions overlap the kernels of other chunks
+// and consecutive kernels overlap each other's tail. The device copy keeps
+// the host layout; a chunk is a strided view of it, computed by
+// fa_fwd_strided.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -23,6 +26,7 @@ struct HostStreams {
   std::once_flag once;
   cudaError_t err = cudaSuccess;
   cudaStream_t in = nullptr, out = nullptr;   // copy-in and copy-out streams of this device
+  cudaStream_t comp = nullptr;                 // kernels of every other chunk (the caller's stream runs the rest)
 };
 HostStreams g_streams[kMaxDevices];
 
@@ -31,6 +35,7 @@ HostStreams* streams_for(int dev) {
   std::call_once(h.once, [&] {
     h.err = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking);
     if (h.err == cudaSuccess) h.err = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking);
+    if (h.err == cudaSuccess) h.err = cudaStreamCreateWithFlags(&h.comp, cudaStreamNonBlocking);
   });
   return h.err == cudaSuccess ? &h : nullptr;
 }
@@ -63,40 +68,76 @@ void offsets(const Layout& l, unsigned long long off[5], unsigned long long* tot
   *total = at;
 }
 
-// A chunk: batches [b0, b1) x KV heads [h0, h1) (query heads [h0 G, h1 G)).
+// A chunk: batches [b0, b1) x query rows [r0, r1) x KV heads [h0, h1) (query
+// heads [h0 G, h1 G)). Its kernel sees keys [0, lim); the chunk copies keys
+// [k0, k1) of its batches and KV heads in (the keys the chunks of the same
+// heads before it did not copy).
 struct Chunk {
-  int b0, b1, h0, h1;
+  int b0, b1, r0, r1, lim, k0, k1, h0, h1;
 };
 
-// Up to four chunks of nearly equal size, over batches when there are enough
-// of them, else over KV heads (all batches at once); one chunk per 48 MiB of
-// copies at most, since a small chunk's kernel leaves SMs idle and its copies
-// are too short to hide anything.
-int plan_chunks(int B, int Hkv, long long copy_bytes, Chunk* c) {
-  const int by_size = static_cast<int>(std::max(1LL, std::min<long long>(4, copy_bytes / (48LL << 20))));
-  if (B >= 2) {
-    const int n = std::min({B, kMaxChunks / 2, by_size});
-    for (int i = 0; i < n; ++i) c[i] = {B * i / n, B * (i + 1) / n, 0, Hkv};
+// Keys row i may see: all of them, or up to i + Sk - Sq (bottom-right mask).
+long long visible(long long i, int Sq, int Sk, int causal) {
+  if (!causal) return Sk;
+  return std::max(0LL, std::min<long long>(Sk, i + Sk - Sq + 1));
+}
+
+// The chunk plan, at most one chunk per 32 MiB of copies (a small chunk's
+// kernel leaves SMs idle and its copies are too short to hide anything):
+//  * four or more batches: ranges of batches;
+//  * else up to four ranges of KV heads, each cut into up to two ranges of
+//    query rows (at a 128-row tile). With a causal mask the first rows see
+//    fewer keys, so the first row range copies only the keys it needs and the
+//    second the rest. Timed end to end on the 16K causal GQA workload (B = 1,
+//    4 KV heads) this plan beat chunks of rows only (1 to 16 of them) and of
+//    heads only.
+int plan_chunks(int B, int Sq, int Sk, int Hkv, int causal, long long copy_bytes, Chunk* c) {
+  const int by_size = static_cast<int>(std::max(1LL, std::min<long long>(kMaxChunks, copy_bytes / (32LL << 20))));
+  if (B >= 4) {
+    const int n = std::min(B, by_size);
+    for (int i = 0; i < n; ++i) c[i] = {B * i / n, B * (i + 1) / n, 0, Sq, Sk, 0, Sk, 0, Hkv};
     return n;
   }
-  const int n = std::min({Hkv, kMaxChunks / 2, by_size});
-  for (int i = 0; i < n; ++i) c[i] = {0, B, Hkv * i / n, Hkv * (i + 1) / n};
+  const int nh = std::min({Hkv, 4, by_size});
+  const int tiles = (Sq + 127) / 128;
+  const int nr = std::min({2, tiles, std::max(1, by_size / nh)});
+  int n = 0;
+  for (int hi = 0; hi < nh; ++hi) {
+    const int h0 = Hkv * hi / nh, h1 = Hkv * (hi + 1) / nh;
+    int r0 = 0, kdone = 0;
+    for (int i = 0; i < nr; ++i) {
+      const int r1 = (i + 1 == nr) ? Sq : static_cast<int>(static_cast<long long>(tiles) * (i + 1) / nr) * 128;
+      if (r1 <= r0) continue;
+      const int lim = static_cast<int>(visible(r1 - 1, Sq, Sk, causal));
+      const int k1 = std::max(kdone, lim);
+      c[n++] = {0, B, r0, r1, lim, kdone, k1, h0, h1};
+      kdone = k1;
+      r0 = r1;
+    }
+  }
   return n;
 }
 
-// Copies the box (batches [b0, b1), rows [0, S), heads [h0, h1), D) of a
-// (B, S, H, D) 16-bit tensor between host and device buffers of that layout.
-cudaError_t copy_bshd(void* dst, const void* src, int b0, int b1, int S, int H, int h0, int h1, int D,
-                      cudaMemcpyKind kind, cudaStream_t s) {
-  const size_t row = static_cast<size_t>(H) * D * 2;                      // one (b, s) row
-  const size_t off = (static_cast<size_t>(b0) * S) * row + static_cast<size_t>(h0) * D * 2;
-  const size_t width = static_cast<size_t>(h1 - h0) * D * 2;
-  const size_t rows = static_cast<size_t>(b1 - b0) * S;
-  if (rows == 0 || width == 0) return cudaSuccess;
-  if (width == row)
-    return cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off, rows * row, kind, s);
-  return cudaMemcpy2DAsync(static_cast<char*>(dst) + off, row, static_cast<const char*>(src) + off, row, width, rows,
-                           kind, s);
+// Copies the box (batches [b0, b1), rows [s0, s1), heads [h0, h1), D) of a
+// (B, S, H, D) 16-bit tensor between host and device buffers of that layout:
+// one block when the box is whole batches, else one 2-D copy per batch.
+cudaError_t copy_box(void* dst, const void* src, int b0, int b1, int s0, int s1, int h0, int h1, int S, int H, int D,
+                     cudaMemcpyKind kind, cudaStream_t s) {
+  const size_t row = static_cast<size_t>(H) * D * 2;   // one (b, s) row
+  if (s1 <= s0 || b1 <= b0 || h1 <= h0) return cudaSuccess;
+  if (s0 == 0 && s1 == S && h0 == 0 && h1 == H) {
+    const size_t off = static_cast<size_t>(b0) * S * row;
+    return cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off,
+                           static_cast<size_t>(b1 - b0) * S * row, kind, s);
+  }
+  for (int b = b0; b < b1; ++b) {
+    const size_t off = (static_cast<size_t>(b) * S + s0) * row + static_cast<size_t>(h0) * D * 2;
+    const cudaError_t e =
+        cudaMemcpy2DAsync(static_cast<char*>(dst) + off, row, static_cast<const char*>(src) + off, row,
+                          static_cast<size_t>(h1 - h0) * D * 2, s1 - s0, kind, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -138,11 +179,11 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
   void* dv = ws + off[2];
   void* dout = ws + off[3];
   float* dlse = reinterpret_cast<float*>(ws + off[4]);
-  const int G = Hq / Hkv;
   Chunk ch[kMaxChunks];
-  const int n = plan_chunks(B, Hkv, l.q_bytes + 2 * l.kv_bytes + l.o_bytes + l.lse_bytes, ch);
+  const int n = plan_chunks(B, Sq, Sk, Hkv, causal, l.q_bytes + 2 * l.kv_bytes + l.o_bytes + l.lse_bytes, ch);
+  const int G = Hq / Hkv;
 
-  // events: fork, per chunk (inputs landed, outputs computed), join
+  // events: fork, join, per chunk (inputs landed, outputs computed)
   cudaEvent_t ev[2 + 2 * kMaxChunks];
   int n_ev = 0;
   int rc = FA_OK;
@@ -156,39 +197,44 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
     const long long qs[3] = {static_cast<long long>(Sq) * Hq * D, static_cast<long long>(Hq) * D, D};
     const long long ks[3] = {static_cast<long long>(Sk) * Hkv * D, static_cast<long long>(Hkv) * D, D};
     bool ok = cudaEventRecord(fork, stream) == cudaSuccess && cudaStreamWaitEvent(hs->in, fork, 0) == cudaSuccess &&
-              cudaStreamWaitEvent(hs->out, fork, 0) == cudaSuccess;
-    long long lse_at = 0;   // chunk LSE blocks are packed (B_c, Hq_c, Sq) in the workspace
+              cudaStreamWaitEvent(hs->out, fork, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(hs->comp, fork, 0) == cudaSuccess;
+    long long lse_at = 0;   // each chunk's LSE block is packed (B_c, Hq_c, rows_c) in the workspace
     for (int c = 0; ok && c < n; ++c) {
       const Chunk& x = ch[c];
-      const int bc = x.b1 - x.b0, hk = x.h1 - x.h0, hq = hk * G;
+      const int bc = x.b1 - x.b0, sq = x.r1 - x.r0, hk = x.h1 - x.h0, hq = hk * G;
+      // Consecutive chunks' kernels alternate between two streams, so that
+      // one chunk's last CTAs and the next chunk's first ones share the GPU.
+      cudaStream_t cs = (c & 1) ? hs->comp : stream;
       cudaEvent_t in_done = ev[2 + 2 * c], out_ready = ev[3 + 2 * c];
-      // copy in
-      ok = copy_bshd(dq, q, x.b0, x.b1, Sq, Hq, x.h0 * G, x.h1 * G, D, cudaMemcpyHostToDevice, hs->in) ==
-               cudaSuccess &&
-           (Sk == 0 ||
-            (copy_bshd(dk, k, x.b0, x.b1, Sk, Hkv, x.h0, x.h1, D, cudaMemcpyHostToDevice, hs->in) == cudaSuccess &&
-             copy_bshd(dv, v, x.b0, x.b1, Sk, Hkv, x.h0, x.h1, D, cudaMemcpyHostToDevice, hs->in) == cudaSuccess)) &&
-           cudaEventRecord(in_done, hs->in) == cudaSuccess && cudaStreamWaitEvent(stream, in_done, 0) == cudaSuccess;
+      // copy in: the chunk's Q rows and the keys it newly needs
+      const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+      ok = copy_box(dq, q, x.b0, x.b1, x.r0, x.r1, x.h0 * G, x.h1 * G, Sq, Hq, D, h2d, hs->in) == cudaSuccess &&
+           copy_box(dk, k, x.b0, x.b1, x.k0, x.k1, x.h0, x.h1, Sk, Hkv, D, h2d, hs->in) == cudaSuccess &&
+           copy_box(dv, v, x.b0, x.b1, x.k0, x.k1, x.h0, x.h1, Sk, Hkv, D, h2d, hs->in) == cudaSuccess &&
+           cudaEventRecord(in_done, hs->in) == cudaSuccess && cudaStreamWaitEvent(cs, in_done, 0) == cudaSuccess;
       if (!ok) break;
-      // compute the chunk: strided views into the device copy
-      const long long qo = (static_cast<long long>(x.b0) * Sq * Hq + static_cast<long long>(x.h0) * G) * D * 2;
+      // the kernel on strided views of the device copy: rows [r0, r1) against
+      // keys [0, lim), which keeps the bottom-right mask (lim - sq = r0 + Sk - Sq)
+      const long long qo = ((static_cast<long long>(x.b0) * Sq + x.r0) * Hq + static_cast<long long>(x.h0) * G) * D * 2;
       const long long ko = (static_cast<long long>(x.b0) * Sk * Hkv + x.h0) * static_cast<long long>(D) * 2;
       float* lse_c = dlse + lse_at;
       rc = fa_fwd_strided(static_cast<char*>(dq) + qo, static_cast<char*>(dk) + ko, static_cast<char*>(dv) + ko,
-                          static_cast<char*>(dout) + qo, lse ? lse_c : nullptr, bc, Sq, Sk, hq, hk, D, qs, ks, ks, qs,
-                          scale, causal, dtype, stream);
+                          static_cast<char*>(dout) + qo, lse ? lse_c : nullptr, bc, sq, x.lim, hq, hk, D, qs, ks, ks,
+                          qs, scale, causal, dtype, cs);
       if (rc != FA_OK) break;
-      ok = cudaEventRecord(out_ready, stream) == cudaSuccess && cudaStreamWaitEvent(hs->out, out_ready, 0) == cudaSuccess;
-      // copy out
-      ok = ok && copy_bshd(o, dout, x.b0, x.b1, Sq, Hq, x.h0 * G, x.h1 * G, D, cudaMemcpyDeviceToHost, hs->out) ==
-                     cudaSuccess;
-      if (ok && lse) {
-        const size_t width = static_cast<size_t>(hq) * Sq * 4, pitch = static_cast<size_t>(Hq) * Sq * 4;
-        char* dst = reinterpret_cast<char*>(lse) + static_cast<size_t>(x.b0) * pitch +
-                    static_cast<size_t>(x.h0) * G * Sq * 4;
-        ok = cudaMemcpy2DAsync(dst, pitch, lse_c, width, width, bc, cudaMemcpyDeviceToHost, hs->out) == cudaSuccess;
+      ok = cudaEventRecord(out_ready, cs) == cudaSuccess && cudaStreamWaitEvent(hs->out, out_ready, 0) == cudaSuccess;
+      // copy out: O rows, and the LSE block into its (B, Hq, Sq) place
+      ok = ok && copy_box(o, dout, x.b0, x.b1, x.r0, x.r1, x.h0 * G, x.h1 * G, Sq, Hq, D, cudaMemcpyDeviceToHost,
+                          hs->out) == cudaSuccess;
+      for (int b = x.b0; ok && lse && b < x.b1; ++b) {
+        const size_t width = static_cast<size_t>(sq) * 4;
+        char* dst = reinterpret_cast<char*>(lse) + ((static_cast<size_t>(b) * Hq + static_cast<size_t>(x.h0) * G) * Sq + x.r0) * 4;
+        const float* srcb = lse_c + static_cast<size_t>(b - x.b0) * hq * sq;
+        ok = cudaMemcpy2DAsync(dst, static_cast<size_t>(Sq) * 4, srcb, width, width, hq, cudaMemcpyDeviceToHost,
+                               hs->out) == cudaSuccess;
       }
-      lse_at += static_cast<long long>(bc) * hq * Sq;
+      lse_at += static_cast<long long>(bc) * hq * sq;
     }
     // join: the caller's stream continues once every copy-out has finished
     const bool joined = cudaEventRecord(join, hs->out) == cudaSuccess && cudaStreamWaitEvent(stream, join, 0) == cudaSuccess;

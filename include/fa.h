@@ -188,13 +188,15 @@ int fa_fwd_host_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D, un
  * fa_fwd_host_workspace_size(...) bytes, 256-byte aligned, owned by the
  * caller and not read before being written.
  *
- * The call splits the problem into up to four chunks (ranges of batches, or
- * when B = 1 ranges of KV heads with their query heads; at most one chunk
- * per 48 MiB of copies, so small problems run as one) and pipelines, per
- * chunk, the host-to-device copy of its Q, K, V, the attention kernel and the
- * device-to-host copy of its O and LSE: copies run on two streams of the
- * library (one per direction, created once per device), kernels on `stream`,
- * ordered by events. It returns after enqueueing; o and lse are complete
+ * The call splits the problem into up to eight chunks (ranges of batches
+ * when B >= 4, else up to four ranges of KV heads times up to two ranges of
+ * query rows; at most one chunk per 32 MiB of copies, so small problems run
+ * as one) and pipelines, per chunk, the host-to-device copy of its Q and of
+ * the K/V rows it newly needs (with a causal mask early rows need only the
+ * first keys), the attention kernel and the device-to-host copy of its O and
+ * LSE: copies run on two streams of the library (one per direction), kernels
+ * alternately on `stream` and a third library stream (streams created once
+ * per device), ordered by events. It returns after enqueueing; o and lse are complete
  * once `stream` has completed (the call makes `stream` wait for the last
  * copy). Overlapping calls on one device share the library's copy streams
  * and so run one after another; they must not share a workspace.

@@ -98,11 +98,17 @@ def test_host_entry_no_keys():
     assert torch.all(o == 0) and torch.all(lse == float("-inf"))
 
 
-# Problems above 48 MiB of copies run as several chunks: three uneven chunks
-# of KV heads (B = 1), and two chunks of batches.
+# Problems above 32 MiB of copies run as several chunks: ranges of KV heads
+# (four, and three uneven ones), two row halves of one KV head with the keys
+# each newly needs, a first row half that sees no key at all (Sq > Sk,
+# causal), chunks of batches (B >= 4), and a mask-free problem.
 LARGE = [
     W(1, 8192, 8192, 32, 4, 128, seed=35),
+    W(1, 6000, 2000, 32, 8, 128, seed=37),
+    W(1, 16384, 16384, 8, 1, 128, seed=39),
+    W(1, 12000, 4000, 16, 1, 128, seed=40),
     W(4, 2048, 2048, 16, 8, 128, seed=36),
+    W(2, 4096, 1024, 16, 4, 128, causal=False, seed=38),
 ]
 
 
@@ -112,8 +118,8 @@ def test_host_entry_in_several_chunks(w):
     q, k, v = (t.pin_memory() for t in draw_inputs(w))
     assert api.fa_debug_set_schedule(0) == api.FA_OK
     try:
-        o_h, l_h = api.fa_fwd_host(q, k, v, causal=True)
-        o_d, l_d = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+        o_h, l_h = api.fa_fwd_host(q, k, v, causal=w.causal)
+        o_d, l_d = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=w.causal)
         torch.cuda.synchronize()
     finally:
         api.fa_debug_set_schedule(-1)
@@ -126,7 +132,7 @@ def test_host_entry_in_several_chunks(w):
     got_o, got_l, ref_o, ref_l = [], [], [], []
     for b in range(w.B):
         for hq in (0, w.Hq - 1):
-            ro, rl = oracle.attention_rows(qf, kf, vf, w.scale, True, b, hq, rows)
+            ro, rl = oracle.attention_rows(qf, kf, vf, w.scale, w.causal, b, hq, rows)
             got_o.append(o_h[b, rows, hq].float().numpy())
             got_l.append(l_h[b, hq, rows].numpy())
             ref_o.append(ro)
