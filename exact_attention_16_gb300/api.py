@@ -26,6 +26,7 @@ __all__ = [
     "fa_fwd_decode_noalloc",
     "fa_fwd_host",
     "fa_fwd_host_workspace_size",
+    "fa_decode_splits",
     "fa_status",
     "fa_status_string",
     "fa_version",
@@ -74,6 +75,7 @@ EXPORTED_SYMBOLS = {
     "fa_debug_set_fault": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "fa_debug_set_schedule": (ctypes.c_int, [ctypes.c_int]),
     "fa_fwd_host_workspace_size": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_decode_splits": (ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_int)]),
     "fa_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6
                     + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_ulonglong,
                        ctypes.c_void_p]),
@@ -313,6 +315,15 @@ def fa_fwd_decode_noalloc(q, k, v, *, scale=None, causal=False, num_splits=0, ou
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_decode_noalloc")
     return out, lse
+
+
+def fa_decode_splits(B, Sq, Sk, Hq, Hkv, D, num_splits=0, num_sms=152) -> int:
+    """Key ranges fa_fwd_decode would use on a GPU with ``num_sms`` SMs (host only)."""
+    out = ctypes.c_int(0)
+    rc = lib().fa_decode_splits(B, Sq, Sk, Hq, Hkv, D, num_splits, num_sms, ctypes.byref(out))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_decode_splits")
+    return int(out.value)
 
 
 def fa_fwd_host_workspace_size(B, Sq, Sk, Hq, Hkv, D) -> int:

@@ -122,9 +122,10 @@ int fa_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o, 
  * GPU with fa_fwd). The Hq/Hkv query heads of a KV group times
  * floor(128 / (Hq/Hkv)) query positions form one row tile, so Hq/Hkv <= 128
  * is required (else FA_ERR_UNSUPPORTED). The keys are cut into `num_splits`
- * ranges of whole 128-key tiles (num_splits <= 0 picks about two waves of
- * CTAs on the current device; the count is clamped to the number of key
- * tiles), each range gives a normalised partial (O_s, LSE_s), and fa_merge's
+ * ranges of whole 128-key tiles (num_splits <= 0 picks the most splits
+ * that keep all CTAs in one wave on the current device's SMs, at least one;
+ * the count is clamped to the number of key tiles), each range gives a
+ * normalised partial (O_s, LSE_s), and fa_merge's
  * rule combines them into O and LSE. Layouts, dtypes, mask and errors as for
  * fa_fwd (contiguous tensors).
  * workspace        device scratch of at least the size returned by
@@ -146,6 +147,15 @@ int fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* l
  */
 int fa_decode_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D, int num_splits,
                              unsigned long long* bytes);
+
+/*
+ * fa_decode_splits — the number of key ranges fa_fwd_decode would use for
+ * these sizes and `num_splits` on a GPU with `num_sms` SMs, without touching
+ * any GPU (host arithmetic only). FA_ERR_INVALID_ARG for a null `n_splits`,
+ * num_sms <= 0, or sizes with nothing to split (B, Sq, Hq or Sk zero); other
+ * argument errors as fa_fwd_decode.
+ */
+int fa_decode_splits(int B, int Sq, int Sk, int Hq, int Hkv, int D, int num_splits, int num_sms, int* n_splits);
 
 /*
  * fa_fwd_decode_noalloc — fa_fwd_decode without a caller-provided workspace,
