@@ -138,9 +138,9 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   p.n_kv_tiles = pl.n_tiles;
   p.timeout_ns = timeout_ns();
   p.status = status_word;
-  const long long gx = static_cast<long long>(pl.n_splits) * pl.n_row_tiles;
-  if (gx > 0x7fffffffLL || Hkv > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
-  const dim3 grid(static_cast<unsigned>(gx), Hkv, B);
+  const long long n_cta = static_cast<long long>(pl.n_splits) * pl.n_row_tiles * Hkv * B;
+  if (n_cta > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(n_cta));
   // the kernel's head dimension: the smallest of 64, 128, 256 that holds D
   const int Dk = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   int rc;

@@ -12,7 +12,8 @@
 //
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (TMEM lanes 0-127,
 // row r = s_local * G + g), warp 4 TMA producer, warp 5 MMA issuer / TMEM
-// owner. Grid: x = split + n_splits * row tile, y = KV head, z = batch.
+// owner. Grid: one CTA per (split, KV head, batch, row tile) along x, row
+// tiles slowest and in descending order.
 // TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256, 256+D);
 // D = 256 fills all 512.
 #pragma once
@@ -107,8 +108,17 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x % p.n_splits, rt = blockIdx.x / p.n_splits;
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  // One linear CTA index, (split, KV head, batch) fastest and the row tile
+  // slowest and descending: with a causal mask the last row tiles have the
+  // most keys, so the longest CTAs start first and the short ones fill the
+  // tail (the longest-first order of "NVIDIA闪存注意力实操" section
+  // "ProgramId重映射").
+  const long long inner = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
+  const long long cta = blockIdx.x;
+  const int rt = p.n_row_tiles - 1 - static_cast<int>(cta / inner);
+  const int in = static_cast<int>(cta % inner);
+  const int split = in % p.n_splits;
+  const int kvh = (in / p.n_splits) % p.Hkv, b = in / (p.n_splits * p.Hkv);
   const int pos0 = rt * p.P;                                  // first query position of the tile
   const int rows_box = p.G * p.P;                              // rows the Q box fills
   // key tiles this row tile needs (bottom-right causal limit of its last row)
