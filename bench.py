@@ -60,6 +60,37 @@ def measured_peaks() -> dict:
     return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def exp_roofline(flop, D, avg_launch_ms):
+    """The softmax's roof: one exp per unmasked (query, key) pair (FLOPs / 4D)
+    per launch, against the probe-measured MUFU ex2 rate."""
+    peak = ex2_peak_per_s()
+    achieved = flop / (4.0 * D) / (avg_launch_ms * 1e-3)
+    return {"bound": "mufu_ex2", "achieved": round(achieved / 1e9, 1),
+            "peak": round(peak / 1e9, 1) if peak else None, "unit": "Gexp/s",
+            "frac": round(achieved / peak, 4) if peak else None,
+            "peak_source": "ex2 throughput probe on this GPU (libfa_probes.so)" if peak else "probe unavailable"}
+
+
+def ex2_peak_per_s():
+    """MUFU ex2 throughput of the current GPU, measured by the probe library
+    (4 blocks per SM x 256 threads x 8 independent ex2 chains), or None."""
+    import ctypes
+
+    import torch
+
+    path = os.path.join(ROOT, "exact_attention_16_gb300", "_lib", "libfa_probes.so")
+    if not os.path.exists(path):
+        return None
+    lib = ctypes.CDLL(path)
+    lib.fa_probe_ex2_rate.restype = ctypes.c_int
+    lib.fa_probe_ex2_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+    rate = ctypes.c_double(0.0)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    rc = lib.fa_probe_ex2_rate(4 * sms, 2048, ctypes.byref(rate),
+                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return rate.value if rc == 0 else None
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source for this workload (else None)."""
@@ -277,6 +308,7 @@ def run_ours(args, w):
             "kernel": "fa_fwd_kernel",
             "avg_launch_ms": round(avg_launch_ms, 4),
         },
+        "exp_roofline": exp_roofline(flop, w.D, avg_launch_ms),
         "e2e": {
             "value": round(whole_job_tflops(world, flop, e2e_steps, e2e_s * 1e3), 2),
             "unit": "TFLOP/s",

@@ -1,7 +1,9 @@
 // Single-tile probes of the hardware primitives the attention kernel is built
 // on (TMA with 128-byte swizzle, tcgen05.mma with shared-memory and tensor-
-// memory operands, tcgen05.ld/st). Test-only library: each probe runs one CTA
-// on one 128-row tile so a failing primitive is isolated from the pipeline.
+// memory operands, tcgen05.ld/st), and a throughput probe of the MUFU ex2
+// unit that sets the attention softmax's second roof. Test and measurement
+// library: each tile probe runs one CTA on one 128-row tile so a failing
+// primitive is isolated from the pipeline.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -202,4 +204,51 @@ extern "C" int fa_probe_pv(const void* P, const void* V, float* out, int bf16, i
   auto p = static_cast<const uint16_t*>(P);
   return bf16 ? run(probe_pv_kernel<true>, smem, s, err, p, tv, out)
               : run(probe_pv_kernel<false>, smem, s, err, p, tv, out);
+}
+
+namespace {
+
+// Every thread runs 8 independent chains x <- 2^(-x) (values stay in
+// (0.5, 1)), so the MUFU pipe, not the latency of one chain, bounds the time.
+__global__ void __launch_bounds__(256) probe_ex2_kernel(int iters, float* sink) {
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = 0.5f + 0.01f * static_cast<float>(i + (threadIdx.x & 7));
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = fa::ptx::ex2_approx(-x[i]);
+  }
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc += x[i];
+  if (acc == 12345.0f) sink[0] = acc;   // keeps the chains live; never true
+}
+
+}  // namespace
+
+// MUFU ex2 throughput of the current device: `blocks` x 256 threads x `iters`
+// x 8 ex2.approx.ftz.f32 operations, timed with CUDA events on `stream`.
+// *ex2_per_s receives the rate. Returns 0, or 3 on a CUDA error.
+extern "C" int fa_probe_ex2_rate(int blocks, int iters, double* ex2_per_s, void* stream) {
+  if (blocks <= 0 || iters <= 0 || !ex2_per_s) return 1;
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  float* sink = nullptr;
+  cudaEvent_t e0, e1;
+  if (cudaMalloc(&sink, sizeof(float)) != cudaSuccess) return 3;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    cudaFree(sink);
+    return 3;
+  }
+  probe_ex2_kernel<<<blocks, 256, 0, s>>>(iters, sink);   // warm-up
+  cudaEventRecord(e0, s);
+  probe_ex2_kernel<<<blocks, 256, 0, s>>>(iters, sink);
+  cudaEventRecord(e1, s);
+  float ms = 0.0f;
+  const bool ok = cudaEventSynchronize(e1) == cudaSuccess && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess &&
+                  cudaGetLastError() == cudaSuccess && ms > 0.0f;
+  if (ok) *ex2_per_s = static_cast<double>(blocks) * 256.0 * iters * 8.0 / (ms * 1e-3);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaFree(sink);
+  return ok ? 0 : 3;
 }

@@ -76,3 +76,16 @@ def test_probe_pv_matches_p_v(probes, dt, kind):
     got = out.cpu().double().numpy()
     tol = 0.0 if kind == "ints" else 1e-4
     np.testing.assert_allclose(got, ref, rtol=0, atol=tol)
+
+
+def test_probe_ex2_rate_is_plausible(probes):
+    # 152 SMs x 16 to 32 ex2 per clock x ~2 GHz: some 5e12 to 1e13 per second;
+    # accept a wide band around it (the probe sets the softmax's roof in the
+    # bench line)
+    probes.fa_probe_ex2_rate.restype = ctypes.c_int
+    probes.fa_probe_ex2_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                         ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rate = ctypes.c_double(0.0)
+    assert probes.fa_probe_ex2_rate(4 * sms, 512, ctypes.byref(rate), None) == 0
+    assert 1e12 < rate.value < 1e14, rate.value
