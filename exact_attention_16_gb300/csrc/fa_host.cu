@@ -84,7 +84,8 @@ long long visible(long long i, int Sq, int Sk, int causal) {
 
 // The chunk plan, at most one chunk per 32 MiB of copies (a small chunk's
 // kernel leaves SMs idle and its copies are too short to hide anything):
-//  * four or more batches: ranges of batches;
+//  * four or more batches: ranges of batches (each cut into two ranges of
+//    KV heads when the size allows eight chunks);
 //  * else up to four ranges of KV heads, each cut into up to two ranges of
 //    query rows (at a 128-row tile). With a causal mask the first rows see
 //    fewer keys, so the first row range copies only the keys it needs and the
@@ -94,8 +95,12 @@ long long visible(long long i, int Sq, int Sk, int causal) {
 int plan_chunks(int B, int Sq, int Sk, int Hkv, int causal, long long copy_bytes, Chunk* c) {
   const int by_size = static_cast<int>(std::max(1LL, std::min<long long>(kMaxChunks, copy_bytes / (32LL << 20))));
   if (B >= 4) {
-    const int n = std::min(B, by_size);
-    for (int i = 0; i < n; ++i) c[i] = {B * i / n, B * (i + 1) / n, 0, Sq, Sk, 0, Sk, 0, Hkv};
+    const int nb = std::min(B, by_size);
+    const int nh = std::min({Hkv, 2, std::max(1, by_size / nb)});
+    int n = 0;
+    for (int i = 0; i < nb; ++i)
+      for (int h = 0; h < nh; ++h)
+        c[n++] = {B * i / nb, B * (i + 1) / nb, 0, Sq, Sk, 0, Sk, Hkv * h / nh, Hkv * (h + 1) / nh};
     return n;
   }
   const int nh = std::min({Hkv, 4, by_size});

@@ -198,8 +198,9 @@ int fa_fwd_host_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D, un
  * fa_fwd_host_workspace_size(...) bytes, 256-byte aligned, owned by the
  * caller and not read before being written.
  *
- * The call splits the problem into up to eight chunks (ranges of batches
- * when B >= 4, else up to four ranges of KV heads times up to two ranges of
+ * The call splits the problem into up to eight chunks (ranges of batches,
+ * times two ranges of KV heads when eight chunks fit, when B >= 4; else up
+ * to four ranges of KV heads times up to two ranges of
  * query rows; at most one chunk per 32 MiB of copies, so small problems run
  * as one) and pipelines, per chunk, the host-to-device copy of its Q and of
  * the K/V rows it newly needs (with a causal mask early rows need only the
