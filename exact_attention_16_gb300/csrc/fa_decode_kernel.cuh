@@ -288,10 +288,12 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
       for (int c = 0; c < 8; ++c) mq[c] = s[c];
 #pragma unroll
-      for (int c = 8; c < 128; c += 16) {
+      for (int c = 8; c < 120; c += 16) {   // columns 8 .. 119
 #pragma unroll
         for (int q = 0; q < 8; ++q) mq[q] = ptx::max3(mq[q], s[c + 2 * q], s[c + 2 * q + 1]);
       }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mq[q] = fmaxf(mq[q], s[120 + q]);   // columns 120 .. 127
       const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
       const float m_new = fmaxf(m_ref, mx * sl2);
       float alpha = 1.0f;

@@ -607,9 +607,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // row max: eight independent chains of three-input max
         float mq[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mq[c] = s[c];
+        for (int q = 0; q < 8; ++q) mq[q] = fmaxf(s[2 * q], s[2 * q + 1]);   // columns 0 .. 15
 #pragma unroll
-        for (int c = 8; c < 128; c += 16) {
+        for (int c = 16; c < 128; c += 16) {   // columns 16 .. 127
 #pragma unroll
           for (int q = 0; q < 8; ++q) mq[q] = ptx::max3(mq[q], s[c + 2 * q], s[c + 2 * q + 1]);
         }
@@ -712,12 +712,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!(ok = bar_wait(bar_stats_full, act & 1u, abort_flag, p))) break;
         const float m1 = stats[row], l1 = stats[kBM + row], c1 = stats[2 * kBM + row];
         ptx::mbar_arrive(bar_stats_empty);
-        // a slot with l > 0 has a finite m; one with l = 0 contributes nothing
-        const float m = l1 > 0.0f ? (l_exact > 0.0f ? fmaxf(m_ref, m1) : m1) : m_ref;
-        const float a0 = l_exact > 0.0f ? ptx::ex2_approx(m_ref - m) : 0.0f;
-        const float a1 = l1 > 0.0f ? ptx::ex2_approx(m1 - m) : 0.0f;
+        // a slot with a finite m saw a key (and has l >= 1); one whose m is
+        // still -inf contributes nothing
+        const bool seen0 = m_ref != -__int_as_float(0x7f800000), seen1 = m1 != -__int_as_float(0x7f800000);
+        const float m = seen1 ? (seen0 ? fmaxf(m_ref, m1) : m1) : m_ref;
+        const float a0 = seen0 ? ptx::ex2_approx(m_ref - m) : 0.0f;
+        const float a1 = seen1 ? ptx::ex2_approx(m1 - m) : 0.0f;
         const float l_tot = a0 * l_exact + a1 * l1;
-        const bool live = l_tot > 0.0f;
+        const bool live = seen0 || seen1;
         const float inv_l = live ? __frcp_rn(a0 * (l_exact + l_corr) + a1 * (l1 + c1)) : 0.0f;
         const uint64_t f0 = ptx::f2_pack(a0 * inv_l, a0 * inv_l);
         const uint64_t f1 = ptx::f2_pack(a1 * inv_l, a1 * inv_l);
@@ -787,7 +789,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_o_empty + 8 * t);
-      const bool live = l_exact > 0.0f;
+      const bool live = m_ref != -__int_as_float(0x7f800000);   // some key seen: l >= 1
       const float inv_l = live ? __frcp_rn(l_exact + l_corr) : 0.0f;
       // Scale, round to the dtype and stage this warp's 32 rows one 64-column
       // chunk at a time in the 128-byte-swizzled layout of the O tensor map;

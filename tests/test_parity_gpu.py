@@ -181,3 +181,41 @@ def test_padded_head_dim_strided_bhsd():
     o, lse = api.fa_fwd(qb.transpose(1, 2), kb.transpose(1, 2), vb.transpose(1, 2), scale=w.scale, causal=True)
     assert api.fa_status() == 0
     _oracle_compare(q, k, v, o, lse, w.scale, True)
+
+
+def _far_below_zero(B, Sq, Sk, Hq, Hkv, D, seed=5):
+    """Inputs whose scores all sit near -181 (about -261 in log2 units): every
+    weight 2^(s - m) underflows fp32 unless m comes from the row's own scores,
+    yet the softmax is an ordinary one over score differences of a few units."""
+    g = torch.Generator().manual_seed(seed)
+    q = (4.0 + 0.05 * torch.randn(B, Sq, Hq, D, generator=g)).to(torch.bfloat16)
+    k = (-4.0 + 0.05 * torch.randn(B, Sk, Hkv, D, generator=g)).to(torch.bfloat16)
+    v = torch.randn(B, Sk, Hkv, D, generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["pairs", "keysplit"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_scores_far_below_zero(mode, D):
+    q, k, v = _far_below_zero(1, 300, 300, 4, 2, D)
+    assert api.fa_debug_set_schedule(mode) == api.FA_OK
+    try:
+        o, lse = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+        torch.cuda.synchronize()
+    finally:
+        api.fa_debug_set_schedule(-1)
+    assert api.fa_status() == 0
+    _oracle_compare(q, k, v, o, lse, D ** -0.5, True)
+
+
+def test_scores_far_below_zero_one_tile_kernel():
+    # D = 256 runs the one-tile split-KV kernel; the decode entry splits the keys
+    q, k, v = _far_below_zero(1, 200, 333, 4, 1, 256)
+    o, lse = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    _oracle_compare(q, k, v, o, lse, 256 ** -0.5, True)
+    q1, k1, v1 = _far_below_zero(4, 1, 2000, 8, 2, 128, seed=6)
+    o1, l1 = api.fa_fwd_decode(q1.cuda(), k1.cuda(), v1.cuda(), causal=True, num_splits=3)
+    torch.cuda.synchronize()
+    assert api.fa_status() == 0
+    _oracle_compare(q1, k1, v1, o1, l1, 128 ** -0.5, True)
