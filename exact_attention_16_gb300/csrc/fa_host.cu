@@ -82,21 +82,25 @@ long long visible(long long i, int Sq, int Sk, int causal) {
   return std::max(0LL, std::min<long long>(Sk, i + Sk - Sq + 1));
 }
 
-// The chunk plan, at most one chunk per 32 MiB of copies (a small chunk's
+// The chunk plan, at most one chunk per 24 MiB of copies (a small chunk's
 // kernel leaves SMs idle and its copies are too short to hide anything):
-//  * four or more batches: ranges of batches (each cut into two ranges of
-//    KV heads when the size allows eight chunks);
-//  * else up to four ranges of KV heads, each cut into up to two ranges of
-//    query rows (at a 128-row tile). With a causal mask the first rows see
+//  * two or more batches: ranges of batches, each cut into up to four ranges
+//    of KV heads while the size allows;
+//  * one batch: up to four ranges of KV heads, each cut into up to two ranges
+//    of query rows (at a 128-row tile). With a causal mask the first rows see
 //    fewer keys, so the first row range copies only the keys it needs and the
-//    second the rest. Timed end to end on the 16K causal GQA workload (B = 1,
-//    4 KV heads) this plan beat chunks of rows only (1 to 16 of them) and of
-//    heads only.
+//    second the rest.
+// Timed end to end (GB300, pinned host tensors): on the 16K causal GQA
+// workload (B = 1, 4 KV heads) heads x row halves beat chunks of rows only (1
+// to 16 of them), of heads only, and finer cuts (1383 TFLOP/s against at most
+// 1351); on B = 2, 8K, 8 KV heads, 2 batches x 4 head ranges gave 581 against
+// 540 for 4 head ranges and 513 for 4 x 2 rows; on B = 4, 4K, 8 KV heads,
+// 4 x 2 stays best (386; 4 x 4: 373, 2 x 4: 363).
 int plan_chunks(int B, int Sq, int Sk, int Hkv, int causal, long long copy_bytes, Chunk* c) {
-  const int by_size = static_cast<int>(std::max(1LL, std::min<long long>(kMaxChunks, copy_bytes / (32LL << 20))));
-  if (B >= 4) {
+  const int by_size = static_cast<int>(std::max(1LL, std::min<long long>(kMaxChunks, copy_bytes / (24LL << 20))));
+  if (B >= 2) {
     const int nb = std::min(B, by_size);
-    const int nh = std::min({Hkv, 2, std::max(1, by_size / nb)});
+    const int nh = std::min({Hkv, 4, std::max(1, by_size / nb)});
     int n = 0;
     for (int i = 0; i < nb; ++i)
       for (int h = 0; h < nh; ++h)

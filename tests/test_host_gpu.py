@@ -98,18 +98,20 @@ def test_host_entry_no_keys():
     assert torch.all(o == 0) and torch.all(lse == float("-inf"))
 
 
-# Problems above 32 MiB of copies run as several chunks: ranges of KV heads
-# (four, and three uneven ones), two row halves of one KV head with the keys
-# each newly needs, a first row half that sees no key at all (Sq > Sk,
-# causal), chunks of batches (B >= 4) alone and times two ranges of KV
-# heads, and a mask-free problem.
+# Problems of 48 MiB of copies or more run as several chunks: (B = 1) ranges
+# of KV heads (four, and three uneven ones), two row halves of one KV head
+# with the keys each newly needs, a first row half that sees no key at all
+# (Sq > Sk, causal); (B >= 2) ranges of batches alone and times two or four
+# ranges of KV heads; and a mask-free problem.
 LARGE = [
     W(1, 8192, 8192, 32, 4, 128, seed=35),
-    W(1, 6000, 2000, 32, 8, 128, seed=37),
+    W(1, 5000, 2000, 32, 8, 128, seed=37),
     W(1, 16384, 16384, 8, 1, 128, seed=39),
     W(1, 12000, 4000, 16, 1, 128, seed=40),
     W(4, 2048, 2048, 16, 8, 128, seed=36),
     W(4, 4096, 4096, 32, 8, 128, seed=42),              # batches x two KV-head halves
+    W(2, 4096, 4096, 16, 8, 128, seed=43),              # 2 batches x 2 KV-head ranges
+    W(3, 4096, 4096, 16, 8, 128, seed=44),              # 3 batches x 2 KV-head ranges
     W(2, 4096, 1024, 16, 4, 128, causal=False, seed=38),
 ]
 
