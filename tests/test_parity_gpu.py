@@ -219,3 +219,34 @@ def test_scores_far_below_zero_one_tile_kernel():
     torch.cuda.synchronize()
     assert api.fa_status() == 0
     _oracle_compare(q1, k1, v1, o1, l1, 128 ** -0.5, True)
+
+
+def _random_shapes(n=24, seed=2024):
+    """Seeded random shapes across every argument the path takes: batch,
+    ragged lengths (Sq > Sk and Sq < Sk), GQA groups 1-8, head dims 32-256
+    (padded ones included), both dtypes, causal or not, sharp or flat
+    softmax."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        hkv = int(rng.choice([1, 2, 4]))
+        g = int(rng.choice([1, 2, 3, 4, 8]))
+        d = int(rng.choice([32, 64, 96, 128, 128, 192, 256]))
+        sq = int(rng.integers(1, 700))
+        sk = int(rng.integers(1, 700))
+        out.append(Workload(f"r{i}", int(rng.integers(1, 4)), sq, sk, g * hkv, hkv, d,
+                            str(rng.choice(["bf16", "fp16"])), bool(rng.integers(0, 2)),
+                            float(rng.choice([0.5, 1.0, 2.0])), 1.0, int(rng.integers(1, 1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_shapes_every_element(i):
+    w = _random_shapes()[i]
+    mode = i % 2 if w.D <= 128 else -1   # alternate the forced schedule
+    assert api.fa_debug_set_schedule(mode) == api.FA_OK
+    try:
+        check_full(w)
+    finally:
+        api.fa_debug_set_schedule(-1)
