@@ -169,12 +169,15 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     bool ok = true;
     uint32_t issued = 0;
     if (n > 0 && lane == 0) {
-      const uint64_t pol_kv = ptx::policy_evict_first();   // each K/V byte is read once
+      // K/V stay in L2 while other row tiles of the same KV head will read
+      // them (prefill); in decode (one row tile) each byte is read once
+      const uint64_t pol_kv = p.n_row_tiles > 1 ? ptx::policy_evict_last() : ptx::policy_evict_first();
+      const uint64_t pol_q = ptx::policy_evict_first();
       const uint32_t q_bytes = static_cast<uint32_t>(rows_box) * 128u * L::kChunks;
       ptx::mbar_arrive_expect_tx(bar_q_full, q_bytes);
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
-        ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, pos0, b, pol_kv);
+        ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, pos0, b, pol_q);
       for (int j = 0; ok && j < 2 * n; ++j) {               // K_0, V_0, K_1, V_1, ...
         const uint32_t st = j % kStages, ph = ((j / kStages) & 1u) ^ 1u;
         if (!(ok = dec_wait(bar_kv_empty + 8 * st, ph, abort_flag, p))) break;
