@@ -46,6 +46,8 @@ CASES = [
     (W(2, 1, 1500, 16, 2, 96), 0),               # padded head dims through the split path
     (W(1, 3, 700, 8, 8, 32, "fp16"), 3),
     (W(1, 1, 600, 4, 4, 160), 2),
+    (W(2, 3, 1000, 64, 1, 128), 0),              # MQA, G = 64: 2 positions per tile
+    (W(1, 1, 3000, 128, 1, 128), 3),             # G = 128: one position fills a tile
 ]
 
 

@@ -50,6 +50,8 @@ SMALL = [
     W(1, 384, 384, 4, 2, 256, causal=True),          # D = 256 (one-tile kernel, one key range)
     W(2, 200, 333, 4, 4, 256, "fp16", causal=False),
     W(1, 300, 257, 8, 1, 256, causal=True),          # D = 256, G = 8, Sq > Sk
+    W(1, 300, 400, 32, 1, 128, causal=True),         # MQA, G = 32 (head pairs of one KV head)
+    W(1, 200, 200, 64, 1, 64, "fp16", causal=False),  # MQA, G = 64
 ]
 
 
