@@ -47,7 +47,7 @@ struct DecodeSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 256) ? 2 : (D == 128) ? 5 : 8;
+  static constexpr int kStages = (D == 256) ? 2 : (D == 128) ? 6 : 12;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
