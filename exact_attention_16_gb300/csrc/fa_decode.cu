@@ -75,6 +75,12 @@ int check_args(int B, int Sq, int Sk, int Hq, int Hkv, int D, int dtype) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Pieces a K or V tile is loaded in (the V map's box is 128 / that keys high).
+int ring_pieces(int Dk) {
+  return Dk == 256 ? fa::DecodeSmem<256>::kHalves : Dk == 128 ? fa::DecodeSmem<128>::kHalves
+                                                               : fa::DecodeSmem<64>::kHalves;
+}
+
 template <int D, bool BF16>
 int launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::DecodeParams& p,
                   dim3 grid, cudaStream_t stream) {
@@ -115,10 +121,12 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   const Plan pl = make_plan(B, Sq, Sk, Hq, Hkv, D, num_splits, device_sms());
   if (pl.n_splits > 1 && (workspace_bytes < pl.workspace_bytes() || !o_part || !lse_part)) return FA_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
+  // the kernel's head dimension: the smallest of 64, 128, 256 that holds D
+  const int Dk = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   CUtensorMap tq, tk, tv;
   if (!encode_bshd_box(&tq, q, bf16, B, Sq, Hq, D, qs, G, pl.positions) ||
       !encode_bshd_box(&tk, k, bf16, B, Sk, Hkv, D, ks, 1, 128) ||
-      !encode_bshd_box(&tv, v, bf16, B, Sk, Hkv, D, vs, 1, 128))
+      !encode_bshd_box(&tv, v, bf16, B, Sk, Hkv, D, vs, 1, 128 / ring_pieces(Dk)))
     return FA_ERR_CUDA;
   DecodeParams p{};
   p.o = o;
@@ -141,8 +149,6 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   const long long n_cta = static_cast<long long>(pl.n_splits) * pl.n_row_tiles * Hkv * B;
   if (n_cta > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(n_cta));
-  // the kernel's head dimension: the smallest of 64, 128, 256 that holds D
-  const int Dk = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   int rc;
   if (Dk == 256)
     rc = bf16 ? launch_decode<256, true>(tq, tk, tv, p, grid, stream)

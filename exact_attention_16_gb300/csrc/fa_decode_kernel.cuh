@@ -47,10 +47,17 @@ struct DecodeSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 256) ? 2 : (D == 128) ? 6 : 12;
+  // Ring unit: a whole K or V tile, or for D = 256 half of one (K: 128 of
+  // its 256 columns; V: 64 of its 128 keys), so that beside the 64 KB Q tile
+  // five 32 KB units fit instead of two 64 KB tiles and each load has about
+  // two MMA groups to land instead of one.
+  static constexpr int kHalves = (D == 256) ? 2 : 1;
+  static constexpr int kUnitBytes = kTileBytes / kHalves;
+  static constexpr int kVChunkBytes = kChunkBytes / kHalves;   // one 64-column chunk of a V unit
+  static constexpr int kStages = (D == 256) ? 5 : (D == 128) ? 6 : 12;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kUnitBytes;
   // q_full, kv_full[S], kv_empty[S], s_full[2], p_full, pv_done, o_full, teardown
   static constexpr int kNumBars = 1 + 2 * kStages + 2 + 1 + 1 + 1 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -86,6 +93,7 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ DecodeParams p) {
   using L = DecodeSmem<D>;
   constexpr int kStages = L::kStages;
+  constexpr int kHalves = L::kHalves;
   constexpr uint32_t kTmemCols = 512;
   constexpr float kRescale = 8.0f;
   const float kNegInf = -__int_as_float(0x7f800000);
@@ -178,15 +186,27 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
         ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, pos0, b, pol_q);
-      for (int j = 0; ok && j < 2 * n; ++j) {               // K_0, V_0, K_1, V_1, ...
-        const uint32_t st = j % kStages, ph = ((j / kStages) & 1u) ^ 1u;
+      // units in order K_0, V_0, K_1, V_1, ... (each in kHalves pieces)
+      for (int u = 0; ok && u < 2 * kHalves * n; ++u) {
+        const uint32_t st = u % kStages, ph = ((u / kStages) & 1u) ^ 1u;
         if (!(ok = dec_wait(bar_kv_empty + 8 * st, ph, abort_flag, p))) break;
-        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * st, L::kTileBytes);
-        const CUtensorMap* map = (j & 1) ? &tm_v : &tm_k;
+        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * st, L::kUnitBytes);
+        const int jt = u / (2 * kHalves), h = u % kHalves, key0 = (t_begin + jt) * 128;
+        const uint32_t dst = sKV + st * L::kUnitBytes;
+        if ((u / kHalves) % 2 == 0) {
+          // K: column chunks h * kChunks / kHalves ..., all 128 keys
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_4d(sKV + st * L::kTileBytes + c * L::kChunkBytes, map, bar_kv_full + 8 * st, c * 64, kvh,
-                           (t_begin + j / 2) * 128, b, pol_kv);
+          for (int c = 0; c < L::kChunks / kHalves; ++c)
+            ptx::tma_load_4d(dst + c * L::kChunkBytes, &tm_k, bar_kv_full + 8 * st,
+                             (h * L::kChunks / kHalves + c) * 64, kvh, key0, b, pol_kv);
+        } else {
+          // V: every column chunk of keys key0 + h * 128 / kHalves ... (the V
+          // map's box is 128 / kHalves keys high)
+#pragma unroll
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_4d(dst + c * L::kVChunkBytes, &tm_v, bar_kv_full + 8 * st, c * 64, kvh,
+                             key0 + h * (128 / kHalves), b, pol_kv);
+        }
         ++issued;
       }
       if (!ok) {
@@ -200,68 +220,76 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    // Lane 0 alone runs the loop (no warp-wide waits or reconvergence
+    // between MMA groups); each ring unit is waited for and released in turn.
     constexpr uint32_t idesc_s = ptx::idesc_f16(BF16, 128, 128, false, false);
     constexpr uint32_t idesc_o = ptx::idesc_f16(BF16, 128, D, false, true);
     const uint64_t dq = ptx::sdesc_sw128(sQ, 16, 1024);
     const uint64_t dk0 = ptx::sdesc_sw128(sKV, 16, 1024);
-    const uint64_t dv0 = ptx::sdesc_sw128(sKV, L::kChunkBytes, 1024);
-    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;
-    bool ok = true;
-    auto wait_load = [&](int j) -> bool {   // j-th load: K_{j/2} or V_{j/2}
-      return dec_wait(bar_kv_full + 8 * (j % kStages), (j / kStages) & 1u, abort_flag, p);
-    };
-    auto issue_s = [&](int jt) {            // S buffer jt%2 = Q K_jt^T
-      const uint32_t st = (2 * jt) % kStages;
+    const uint64_t dv0 = ptx::sdesc_sw128(sKV, L::kVChunkBytes, 1024);   // V: MN-major, chunk stride
+    constexpr uint32_t kUnitDesc = L::kUnitBytes >> 4;
+    constexpr int kS = D / 16;                  // k-steps of Q K^T (16 columns each)
+    constexpr int kSU = kS / kHalves;           // ... per K unit
+    constexpr int kPVU = 8 / kHalves;           // k-steps of P V (16 keys each) per V unit
+    if (lane == 0 && n > 0) {
+      bool ok = true;
+      auto wait_unit = [&](int u) -> bool {   // ring unit u (see the producer)
+        return dec_wait(bar_kv_full + 8 * (u % kStages), (u / kStages) & 1u, abort_flag, p);
+      };
+      // S buffer jt%2 = Q K_jt^T
+      auto issue_s = [&](int jt) -> bool {
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = static_cast<uint32_t>(((ks / 4) * L::kChunkBytes + (ks % 4) * 32) >> 4);
-        ptx::mma_ss(tmem + 128 * (jt & 1), dq + off, dk0 + st * kStageDesc + off, idesc_s, ks > 0 ? 1u : 0u);
-      }
-      ptx::mma_commit(bar_s_full + 8 * (jt & 1));
-      ptx::mma_commit(bar_kv_empty + 8 * st);
-    };
-    if (n > 0) {
-      ok = dec_wait(bar_q_full, 0, abort_flag, p) && wait_load(0);
-      if (ok) {
-        ptx::tc_fence_after();
-        if (lane == 0) issue_s(0);
-        __syncwarp();
-      }
-      if (ok && n > 1 && (ok = wait_load(2))) {
-        ptx::tc_fence_after();
-        if (lane == 0) issue_s(1);
-        __syncwarp();
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        if (!(ok = dec_wait(bar_p_full, j & 1, abort_flag, p) && wait_load(2 * j + 1))) break;
-        ptx::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t vst = (2 * j + 1) % kStages;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            ptx::mma_ts(tmem + 256, tmem + 128 * (j & 1) + ks * 8,
-                        dv0 + vst * kStageDesc + static_cast<uint32_t>((ks * 16 * 128) >> 4), idesc_o,
-                        (j == 0 && ks == 0) ? 0u : 1u);
-          ptx::mma_commit(bar_pv_done);
-          ptx::mma_commit(bar_kv_empty + 8 * vst);
-          if (j + 1 == n) ptx::mma_commit(bar_o_full);
-        }
-        __syncwarp();
-        if (j + 2 < n) {
-          if (!(ok = wait_load(2 * (j + 2)))) break;
+        for (int h = 0; h < kHalves; ++h) {
+          const int u = 2 * kHalves * jt + h;
+          const uint32_t st = u % kStages;
+          if (!wait_unit(u)) return false;
           ptx::tc_fence_after();
-          if (lane == 0) issue_s(j + 2);
-          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < kSU; ++k) {
+            const int ks = h * kSU + k;
+            const uint32_t qoff = static_cast<uint32_t>(((ks / 4) * L::kChunkBytes + (ks % 4) * 32) >> 4);
+            const uint32_t koff = static_cast<uint32_t>(((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
+            ptx::mma_ss(tmem + 128 * (jt & 1), dq + qoff, dk0 + st * kUnitDesc + koff, idesc_s, ks > 0 ? 1u : 0u);
+          }
+          if (h + 1 == kHalves) ptx::mma_commit(bar_s_full + 8 * (jt & 1));
+          ptx::mma_commit(bar_kv_empty + 8 * st);
         }
+        return true;
+      };
+      ok = dec_wait(bar_q_full, 0, abort_flag, p) && issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n; ++j) {
+        if (!(ok = dec_wait(bar_p_full, j & 1, abort_flag, p))) break;
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h) {
+          const int u = 2 * kHalves * j + kHalves + h;
+          const uint32_t vst = u % kStages;
+          if (!(ok = wait_unit(u))) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kPVU; ++k) {
+            const int ks = h * kPVU + k;
+            ptx::mma_ts(tmem + 256, tmem + 128 * (j & 1) + ks * 8,
+                        dv0 + vst * kUnitDesc + static_cast<uint32_t>((k * 16 * 128) >> 4), idesc_o,
+                        (j == 0 && ks == 0) ? 0u : 1u);
+          }
+          if (h + 1 == kHalves) {
+            ptx::mma_commit(bar_pv_done);
+            if (j + 1 == n) ptx::mma_commit(bar_o_full);
+          }
+          ptx::mma_commit(bar_kv_empty + 8 * vst);
+        }
+        if (ok && j + 2 < n) ok = issue_s(j + 2);
       }
       if (!ok) {
-        if (lane == 0) ptx::mma_commit(bar_teardown);
-        __syncwarp();
+        // Wait (bounded) for every MMA already issued before TMEM is released.
+        ptx::mma_commit(bar_teardown);
         const uint64_t t0 = ptx::globaltimer_ns();
         while (!ptx::mbar_try_wait(bar_teardown, 0) && ptx::globaltimer_ns() - t0 < 2000000ull) {
         }
       }
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int row = threadIdx.x;                    // TMEM lane
