@@ -216,7 +216,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_init(bar_q_full + 8 * t, 1);
       ptx::mbar_init(bar_q_empty + 8 * t, 1);
       ptx::mbar_init(bar_s_full + 8 * t, 1);
-      ptx::mbar_init(bar_p_full + 8 * t, 128);
+      ptx::mbar_init(bar_p_full + 8 * t, 4);   // one arrival per softmax warp
       ptx::mbar_init(bar_o_full + 8 * t, 1);
       ptx::mbar_init(bar_o_empty + 8 * t, 128);
     }
@@ -691,9 +691,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           ptx::f2_unpack(ptx::f2_add(acc0, acc1), a0, a1);
           l_exact += a0 + a1;
         }
+        // every lane's P stores complete, then one arrival for the warp
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_p_full + 8 * t);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_p_full + 8 * t);
       }
       if (!ok) break;
       if constexpr (KSPLIT) {
