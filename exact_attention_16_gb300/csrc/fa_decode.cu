@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -144,6 +145,15 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.n_splits = pl.n_splits;
   p.n_kv_tiles = pl.n_tiles;
+  {
+    // CTAs of units whose K/V (one split's key range) fit in 32 MiB together
+    // run interleaved, so the row tiles reading them hit L2
+    const long long keys = static_cast<long long>((pl.n_tiles + pl.n_splits - 1) / pl.n_splits) * 128;
+    const long long unit_bytes = 2LL * keys * D * 2;
+    const long long n_units = static_cast<long long>(pl.n_splits) * Hkv * B;
+    const long long fit = unit_bytes > 0 ? (32LL << 20) / unit_bytes : n_units;
+    p.unit_group = static_cast<int>(std::max(1LL, std::min(n_units, fit)));
+  }
   p.timeout_ns = timeout_ns();
   p.status = status_word;
   const long long n_cta = static_cast<long long>(pl.n_splits) * pl.n_row_tiles * Hkv * B;

@@ -38,6 +38,7 @@ struct DecodeParams {
   int causal;
   float scale_log2;
   int n_splits, n_kv_tiles;
+  int unit_group;      // (split, KV head, batch) units whose CTAs run interleaved
   unsigned long long timeout_ns;
   int* status;
 };
@@ -116,15 +117,20 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One linear CTA index, (split, KV head, batch) fastest and the row tile
-  // slowest and descending: with a causal mask the last row tiles have the
-  // most keys, so the longest CTAs start first and the short ones fill the
-  // tail (the longest-first order of "NVIDIA闪存注意力实操" section
-  // "ProgramId重映射").
-  const long long inner = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
+  // One linear CTA index. Units (split, KV head, batch) go in groups of
+  // unit_group whose K/V fit in L2 together; within a group the unit is
+  // fastest and the row tile slowest and descending: with a causal mask the
+  // last row tiles have the most keys, so the longest CTAs start first and
+  // the short ones fill the tail (the longest-first order of "NVIDIA闪存注意力
+  // 实操" section "ProgramId重映射").
+  const long long n_units = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
   const long long cta = blockIdx.x;
-  const int rt = p.n_row_tiles - 1 - static_cast<int>(cta / inner);
-  const int in = static_cast<int>(cta % inner);
+  const long long group_ctas = static_cast<long long>(p.unit_group) * p.n_row_tiles;
+  const long long g0 = (cta / group_ctas) * p.unit_group;   // first unit of this CTA's group
+  const long long in_group = n_units - g0 < p.unit_group ? n_units - g0 : p.unit_group;
+  const long long w_in = cta - g0 * p.n_row_tiles;
+  const int rt = p.n_row_tiles - 1 - static_cast<int>(w_in / in_group);
+  const int in = static_cast<int>(g0 + w_in % in_group);
   const int split = in % p.n_splits;
   const int kvh = (in / p.n_splits) % p.Hkv, b = in / (p.n_splits * p.Hkv);
   const int pos0 = rt * p.P;                                  // first query position of the tile
