@@ -21,7 +21,7 @@ import math
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "by_name", "draw_inputs", "draw_numpy"]
+__all__ = ["Workload", "WORKLOADS", "by_name", "draw_inputs", "draw_numpy", "draw_device"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -82,3 +82,19 @@ def draw_inputs(w: Workload):
 
     dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[w.dtype]
     return tuple(torch.from_numpy(a).to(dt) for a in draw_numpy(w))
+
+
+def draw_device(shape, dtype: str, sigma: float, seed: int, device="cuda"):
+    """A tensor too large to draw on the host (several GB): N(0, sigma^2)
+    entries drawn directly in ``dtype`` ("bf16", "fp16" or "fp32") on ``device`` by torch's
+    counter-based (Philox) generator seeded with ``seed``. A consumer that
+    checks it on the host copies back the slices it reads."""
+    import torch
+
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[dtype]
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    t = torch.randn(shape, dtype=dt, device=device, generator=g)
+    if sigma != 1.0:
+        t.mul_(sigma)
+    return t
