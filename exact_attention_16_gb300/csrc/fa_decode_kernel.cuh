@@ -177,6 +177,9 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The merge of the split results may be scheduled from now on: it waits
+  // for this grid's completion before it reads anything.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer

@@ -75,6 +75,10 @@ __global__ void __launch_bounds__(256, 3) merge_kernel(const TP* __restrict__ o_
                                                        const float* __restrict__ lse_parts, int n_parts,
                                                        void* __restrict__ o, float* __restrict__ lse, IDX rows, IDX Sq,
                                                        IDX Hq, IDX D) {
+  // Launched right behind the split-KV kernel that writes the parts, this
+  // grid may start before that one has finished: wait for it (and for its
+  // writes to be visible). Without a programmatic launch this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kE = 16;                                   // output elements per thread
   constexpr int kGroup = sizeof(TP) == 4 ? 2 : 4;          // parts whose loads are in flight together
   constexpr int kChunks = kE / Chunk<TP>::kElems;           // 16-byte loads per part
@@ -140,9 +144,13 @@ __global__ void __launch_bounds__(256, 3) merge_kernel(const TP* __restrict__ o_
   }
 }
 
+// `after_producer`: launched with programmatic stream serialization, so that
+// its CTAs are scheduled while the kernel before it (which signals
+// griddepcontrol.launch_dependents) still runs; merge_kernel's first
+// instruction waits for that kernel's completion.
 template <typename TP, bool OUT_BF16>
 int launch_merge(const TP* o_parts, const float* lse_parts, int n, void* o, float* lse, long long rows, int Sq,
-                 int Hq, int D, cudaStream_t stream) {
+                 int Hq, int D, cudaStream_t stream, bool after_producer = false) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                 cudaSuccess)
@@ -150,13 +158,25 @@ int launch_merge(const TP* o_parts, const float* lse_parts, int n, void* o, floa
   const long long items = rows * (D / 16);
   const long long blocks_needed = (items + 255) / 256;
   const int blocks = static_cast<int>(blocks_needed < 32LL * sms ? blocks_needed : 32LL * sms);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_producer ? 1 : 0;
+  cudaError_t e;
   if (items * 8 + 256LL * blocks < 0x7fffffffLL)   // every index (and the loop bound) fits 32 bits
-    merge_kernel<TP, OUT_BF16, unsigned><<<blocks, 256, 0, stream>>>(
-        o_parts, lse_parts, n, o, lse, static_cast<unsigned>(rows), static_cast<unsigned>(Sq),
-        static_cast<unsigned>(Hq), static_cast<unsigned>(D));
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<TP, OUT_BF16, unsigned>, o_parts, lse_parts, n, o, lse,
+                           static_cast<unsigned>(rows), static_cast<unsigned>(Sq), static_cast<unsigned>(Hq),
+                           static_cast<unsigned>(D));
   else
-    merge_kernel<TP, OUT_BF16, long long><<<blocks, 256, 0, stream>>>(o_parts, lse_parts, n, o, lse, rows, Sq, Hq, D);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<TP, OUT_BF16, long long>, o_parts, lse_parts, n, o, lse, rows,
+                           static_cast<long long>(Sq), static_cast<long long>(Hq), static_cast<long long>(D));
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -167,9 +187,9 @@ int merge_f32_parts(const float* o_parts, const float* lse_parts, int n_parts, v
                     int Hq, int D, int dtype, cudaStream_t stream) {
   const long long rows = static_cast<long long>(B) * Sq * Hq;
   if (rows == 0) return FA_OK;
-  return dtype == FA_DTYPE_BF16 ? launch_merge<float, true>(o_parts, lse_parts, n_parts, o, lse, rows, Sq, Hq, D, stream)
-                                : launch_merge<float, false>(o_parts, lse_parts, n_parts, o, lse, rows, Sq, Hq, D,
-                                                             stream);
+  return dtype == FA_DTYPE_BF16
+             ? launch_merge<float, true>(o_parts, lse_parts, n_parts, o, lse, rows, Sq, Hq, D, stream, true)
+             : launch_merge<float, false>(o_parts, lse_parts, n_parts, o, lse, rows, Sq, Hq, D, stream, true);
 }
 
 }  // namespace fa
