@@ -50,38 +50,34 @@ __device__ void Chunk<__half>::to_float(const uint4& v, float* x) {
 }
 
 template <bool BF16>
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if constexpr (BF16) {
-      const __nv_bfloat162 a = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
-      w[q] = *reinterpret_cast<const uint32_t*>(&a);
-    } else {
-      const __half2 a = __floats2half2_rn(x[2 * q], x[2 * q + 1]);
-      w[q] = *reinterpret_cast<const uint32_t*>(&a);
-    }
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&a);
+  } else {
+    const __half2 a = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&a);
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
-
 
 // o_parts: (n, B, Sq, Hq, D) of TP; lse_parts: (n, B, Hq, Sq) fp32;
 // o: (B, Sq, Hq, D) 16-bit; lse: (B, Hq, Sq) fp32 or null. Each thread owns
-// eight consecutive elements of one row and folds the parts in groups of
-// kGroup with a running max (the online-softmax rescale).
-template <typename TP, bool OUT_BF16, typename IDX>
+// kE consecutive elements of one row and folds the parts in groups of kGroup
+// (loads of a group in flight together) with a running max (the
+// online-softmax rescale). Few rows and many parts (decode of one or a few
+// sequences split over the whole GPU) take kE = 4 and a deep group: four
+// times the threads, and fewer dependent round trips per thread.
+template <typename TP, bool OUT_BF16, typename IDX, int kE, int kGroup>
 __global__ void __launch_bounds__(256, 3) merge_kernel(const TP* __restrict__ o_parts,
-                                                       const float* __restrict__ lse_parts, int n_parts,
-                                                       void* __restrict__ o, float* __restrict__ lse, IDX rows, IDX Sq,
-                                                       IDX Hq, IDX D) {
+                                                    const float* __restrict__ lse_parts, int n_parts,
+                                                    void* __restrict__ o, float* __restrict__ lse, IDX rows, IDX Sq,
+                                                    IDX Hq, IDX D) {
   // Launched right behind the split-KV kernel that writes the parts, this
   // grid may start before that one has finished: wait for it (and for its
   // writes to be visible). Without a programmatic launch this returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int kE = 16;                                   // output elements per thread
-  constexpr int kGroup = sizeof(TP) == 4 ? 2 : 4;          // parts whose loads are in flight together
   constexpr int kChunks = kE / Chunk<TP>::kElems;           // 16-byte loads per part
+  static_assert(kChunks >= 1 && kE % 4 == 0, "a thread loads whole 16-byte chunks");
   const IDX per_row = D / kE;
   const IDX items = rows * per_row;
   const long long part_o = static_cast<long long>(rows) * D;
@@ -129,17 +125,17 @@ __global__ void __launch_bounds__(256, 3) merge_kernel(const TP* __restrict__ o_
     }
     const bool live = m > -INFINITY;
     const float inv = live ? 1.0f / tot : 0.0f;
+    uint32_t w[kE / 2];
 #pragma unroll
-    for (int q = 0; q < kE; ++q) acc[q] *= inv;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(o) + static_cast<long long>(row) * D + e);
-    float lo[8], hi[8];
+    for (int q = 0; q < kE / 2; ++q) w[q] = pack2<OUT_BF16>(acc[2 * q] * inv, acc[2 * q + 1] * inv);
+    uint16_t* dst = static_cast<uint16_t*>(o) + static_cast<long long>(row) * D + e;
+    if constexpr (kE == 4) {
+      __stcs(reinterpret_cast<uint2*>(dst), make_uint2(w[0], w[1]));
+    } else {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      lo[q] = acc[q];
-      hi[q] = acc[8 + q];
+      for (int q = 0; q < kE / 8; ++q)
+        __stcs(reinterpret_cast<uint4*>(dst) + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
     }
-    __stcs(dst, pack8<OUT_BF16>(lo));
-    __stcs(dst + 1, pack8<OUT_BF16>(hi));
     if (lse && e == 0) lse[li] = live ? m + logf(tot) : -INFINITY;
   }
 }
@@ -148,14 +144,10 @@ __global__ void __launch_bounds__(256, 3) merge_kernel(const TP* __restrict__ o_
 // its CTAs are scheduled while the kernel before it (which signals
 // griddepcontrol.launch_dependents) still runs; merge_kernel's first
 // instruction waits for that kernel's completion.
-template <typename TP, bool OUT_BF16>
-int launch_merge(const TP* o_parts, const float* lse_parts, int n, void* o, float* lse, long long rows, int Sq,
-                 int Hq, int D, cudaStream_t stream, bool after_producer = false) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                cudaSuccess)
-    return FA_ERR_CUDA;
-  const long long items = rows * (D / 16);
+template <typename TP, bool OUT_BF16, int kE, int kGroup>
+int launch_merge_e(const TP* o_parts, const float* lse_parts, int n, void* o, float* lse, long long rows, int Sq,
+                   int Hq, int D, int sms, cudaStream_t stream, bool after_producer) {
+  const long long items = rows * (D / kE);
   const long long blocks_needed = (items + 255) / 256;
   const int blocks = static_cast<int>(blocks_needed < 32LL * sms ? blocks_needed : 32LL * sms);
   cudaLaunchAttribute attr[1];
@@ -169,14 +161,36 @@ int launch_merge(const TP* o_parts, const float* lse_parts, int n, void* o, floa
   cfg.attrs = attr;
   cfg.numAttrs = after_producer ? 1 : 0;
   cudaError_t e;
-  if (items * 8 + 256LL * blocks < 0x7fffffffLL)   // every index (and the loop bound) fits 32 bits
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<TP, OUT_BF16, unsigned>, o_parts, lse_parts, n, o, lse,
+  if (rows * D + 256LL * blocks < 0x7fffffffLL)   // every index (and the loop bound) fits 32 bits
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<TP, OUT_BF16, unsigned, kE, kGroup>, o_parts, lse_parts, n, o, lse,
                            static_cast<unsigned>(rows), static_cast<unsigned>(Sq), static_cast<unsigned>(Hq),
                            static_cast<unsigned>(D));
   else
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<TP, OUT_BF16, long long>, o_parts, lse_parts, n, o, lse, rows,
-                           static_cast<long long>(Sq), static_cast<long long>(Hq), static_cast<long long>(D));
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<TP, OUT_BF16, long long, kE, kGroup>, o_parts, lse_parts, n, o, lse,
+                           rows, static_cast<long long>(Sq), static_cast<long long>(Hq), static_cast<long long>(D));
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// `after_producer`: launched with programmatic stream serialization, so that
+// its CTAs are scheduled while the kernel before it (which signals
+// griddepcontrol.launch_dependents) still runs; merge_kernel's first
+// instruction waits for that kernel's completion.
+template <typename TP, bool OUT_BF16>
+int launch_merge(const TP* o_parts, const float* lse_parts, int n, void* o, float* lse, long long rows, int Sq,
+                 int Hq, int D, cudaStream_t stream, bool after_producer = false) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return FA_ERR_CUDA;
+  // fp32 parts with fewer 16-element items than one 256-thread block per SM:
+  // four elements per thread, eight parts in flight
+  if constexpr (sizeof(TP) == 4) {
+    if (rows * (D / 16) < 256LL * sms)
+      return launch_merge_e<TP, OUT_BF16, 4, 8>(o_parts, lse_parts, n, o, lse, rows, Sq, Hq, D, sms, stream,
+                                                after_producer);
+  }
+  return launch_merge_e<TP, OUT_BF16, 16, sizeof(TP) == 4 ? 2 : 4>(o_parts, lse_parts, n, o, lse, rows, Sq, Hq, D,
+                                                                   sms, stream, after_producer);
 }
 
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
