@@ -223,6 +223,69 @@ def test_scores_far_below_zero_one_tile_kernel():
     _oracle_compare(q1, k1, v1, o1, l1, 128 ** -0.5, True)
 
 
+# LSE bound for integer-valued inputs. With q, k integers in [-2, 2) every
+# product q_d k_d is an integer and the fp32 accumulation of D <= 256 of them
+# is exact, so the scores carry no error and the LSE error comes from the
+# softmax arithmetic alone: the fp32 rounding of scale * log2(e) (relative
+# 6e-8 on scaled scores of a few tens), the fp32 sums of at most a few thousand
+# weights per row (a few 1e-6 relative), the approximate exp2 and log2
+# (about 2^-22 relative) and the final (m + log2 l) * ln 2 in fp32 (two
+# roundings of a value below 70). Together these stay below 1.5e-5; the bound
+# keeps a margin of three on top, twenty times tighter than the general 1e-3.
+INT_LSE_MAX_ABS = 5e-5
+
+
+def _integer_inputs(B, Sq, Sk, Hq, Hkv, D, dtype, seed):
+    """Integer-valued q, k, v in [-2, 2) (the integer test inputs of the
+    CuTe-DSL example "ampere/flash_attention_v2.py", whose Q K^T is exact in
+    every precision)."""
+    g = torch.Generator().manual_seed(seed)
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    return tuple(torch.randint(-2, 2, shape, generator=g).to(dt)
+                 for shape in ((B, Sq, Hq, D), (B, Sk, Hkv, D), (B, Sk, Hkv, D)))
+
+
+def _int_lse_check(q, k, v, o, lse, scale, causal):
+    import oracle
+    from parity import compare
+    o_ref, l_ref = oracle.attention(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, causal)
+    got = lse.cpu().numpy().astype(np.float64)
+    compare(o.float().cpu().numpy().transpose(0, 2, 1, 3), got, o_ref.transpose(0, 2, 1, 3), l_ref)
+    live = np.isfinite(l_ref)
+    assert np.array_equal(live, np.isfinite(got))
+    err = float(np.abs(got[live] - l_ref[live]).max()) if live.any() else 0.0
+    assert err <= INT_LSE_MAX_ABS, err
+
+
+@pytest.mark.parametrize("mode,D,dtype,causal", [
+    (0, 128, "bf16", True), (1, 128, "bf16", True), (0, 64, "fp16", False), (1, 64, "fp16", False),
+    (-1, 256, "bf16", True)], ids=["d128_bf16_causal_pairs", "d128_bf16_causal_keysplit", "d64_fp16_pairs",
+                                   "d64_fp16_keysplit", "d256_bf16_causal"])
+def test_integer_inputs_exact_scores(mode, D, dtype, causal):
+    """Exact scores isolate the softmax: O within the general tolerance and
+    LSE within the tighter bound above, for both work decompositions at
+    D = 64 / 128 and for the one-tile kernel that D = 256 runs."""
+    q, k, v = _integer_inputs(2, 300, 421, 8, 2, D, dtype, seed=31 + D)
+    assert api.fa_debug_set_schedule(mode) == api.FA_OK
+    try:
+        o, lse = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+        torch.cuda.synchronize()
+    finally:
+        api.fa_debug_set_schedule(-1)
+    assert api.fa_status() == 0
+    _int_lse_check(q, k, v, o, lse, D ** -0.5, causal)
+
+
+def test_integer_inputs_exact_scores_decode_splits():
+    """The split-KV decode path and its merge of partial states on exact
+    scores: the merged LSE obeys the same bound."""
+    q, k, v = _integer_inputs(3, 2, 3000, 16, 4, 128, "bf16", seed=77)
+    o, lse = api.fa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), causal=True, num_splits=5)
+    torch.cuda.synchronize()
+    assert api.fa_status() == 0
+    _int_lse_check(q, k, v, o, lse, 128 ** -0.5, True)
+
+
 def _random_shapes(n=24, seed=2024):
     """Seeded random shapes across every argument the path takes: batch,
     ragged lengths (Sq > Sk and Sq < Sk), GQA groups 1-8, head dims 32-256
