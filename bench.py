@@ -412,6 +412,17 @@ def run_decode(args, w):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if args.graph:
+        # One step captured in a CUDA graph and replayed: at a few sequences a
+        # step's GPU time is below the host cost of one eager call through
+        # the binding, which the eager loop would otherwise measure.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        step = graph.replay
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -436,6 +447,7 @@ def run_decode(args, w):
         "vs_baseline": None, "dtype": wd.dtype, "data": "synthetic (seeded PCG64 normal draws rounded to the dtype)",
         "config": {"workload": wd.name, "B": wd.B, "Sq": 1, "Sk": wd.Sk, "Hq": wd.Hq, "Hkv": wd.Hkv, "D": wd.D,
                    "bytes_per_step": nbytes, "workspace_bytes": need,
+                   "launch": "CUDA graph replay per step" if args.graph else "eager call per step",
                    "l2": f"K+V {nbytes >> 20} MiB" + (" > 129 MB L2; no flush" if nbytes > L2_BYTES else
                                                        " (smaller than L2: hot-L2 figure)")},
         "roofline": {"bound": "hbm", "achieved": round(nbytes / (avg * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
@@ -599,6 +611,7 @@ def main():
                     help="fwd: the attention forward (default); merge: partial-state merge; decode: split-KV "
                          "decode; splitkv: the workload through the split-KV path")
     ap.add_argument("--decode-batch", type=int, default=16, help="sequences per step for --op decode")
+    ap.add_argument("--graph", action="store_true", help="--op decode: replay each step from a CUDA graph")
     ap.add_argument("--parts", type=int, default=4, help="partial states for --op merge")
     ap.add_argument("--head-dim", type=int, default=0, help="override the workload's head dimension (64/128/256)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[x.name for x in WORKLOADS])
