@@ -223,6 +223,62 @@ def test_scores_far_below_zero_one_tile_kernel():
     _oracle_compare(q1, k1, v1, o1, l1, 128 ** -0.5, True)
 
 
+def test_scores_far_above_zero():
+    """Every score near +181 (about +261 in log2 units): 2^s overflows fp32, so
+    the result is finite only if each weight is taken relative to the row's
+    running max. Both decompositions, the one-tile kernel and decode splits."""
+    q, k, v = _far_below_zero(1, 300, 300, 4, 2, 128, seed=8)
+    k = -k.float()
+    k = k.to(torch.bfloat16)
+    for mode in (0, 1):
+        assert api.fa_debug_set_schedule(mode) == api.FA_OK
+        try:
+            o, lse = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+            torch.cuda.synchronize()
+        finally:
+            api.fa_debug_set_schedule(-1)
+        assert api.fa_status() == 0
+        _oracle_compare(q, k, v, o, lse, 128 ** -0.5, True)
+    q2, k2, v2 = _far_below_zero(2, 100, 700, 8, 2, 256, seed=9)
+    k2 = (-k2.float()).to(torch.bfloat16)
+    o2, l2 = api.fa_fwd(q2.cuda(), k2.cuda(), v2.cuda(), causal=False)
+    torch.cuda.synchronize()
+    _oracle_compare(q2, k2, v2, o2, l2, 256 ** -0.5, False)
+    q3, k3, v3 = _far_below_zero(3, 1, 2000, 8, 2, 128, seed=10)
+    k3 = (-k3.float()).to(torch.bfloat16)
+    o3, l3 = api.fa_fwd_decode(q3.cuda(), k3.cuda(), v3.cuda(), causal=True, num_splits=4)
+    torch.cuda.synchronize()
+    assert api.fa_status() == 0
+    _oracle_compare(q3, k3, v3, o3, l3, 128 ** -0.5, True)
+
+
+@pytest.mark.parametrize("scale", [1e-3, 0.05, 0.5, 3.0], ids=["s1e-3", "s0.05", "s0.5", "s3"])
+def test_explicit_scales(scale):
+    """The scale is an argument, not 1/sqrt(D): near-uniform weights (1e-3)
+    up to near one-hot rows (3.0, scores with a spread of about 34), through
+    each kernel: row-tile pairs (D = 128), key-split items (D = 64), the
+    one-tile kernel (D = 256) and decode splits."""
+    from exact_attention_16_gb300.workloads import draw_inputs
+    cases = [(W(2, 333, 517, 8, 2, 128, causal=True, seed=21), 0, "fwd"),
+             (W(1, 300, 300, 4, 4, 64, "fp16", causal=False, seed=22), 1, "fwd"),
+             (W(1, 200, 333, 4, 1, 256, causal=True, seed=23), -1, "fwd"),
+             (W(4, 1, 3000, 16, 4, 128, causal=True, seed=24), -1, "decode")]
+    for w, mode, entry in cases:
+        q, k, v = draw_inputs(w)
+        assert api.fa_debug_set_schedule(mode) == api.FA_OK
+        try:
+            if entry == "fwd":
+                o, lse = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=w.causal)
+            else:
+                o, lse = api.fa_fwd_decode(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=w.causal,
+                                           num_splits=5)
+            torch.cuda.synchronize()
+        finally:
+            api.fa_debug_set_schedule(-1)
+        assert api.fa_status() == 0
+        _oracle_compare(q, k, v, o, lse, scale, w.causal)
+
+
 # LSE bound for integer-valued inputs. With q, k integers in [-2, 2) every
 # product q_d k_d is an integer and the fp32 accumulation of D <= 256 of them
 # is exact, so the scores carry no error and the LSE error comes from the
