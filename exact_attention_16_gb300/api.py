@@ -150,6 +150,38 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype}; expected torch.bfloat16 or torch.float16")
 
 
+def _check_result(name, t, shape, dtype, device):
+    """A caller-supplied result buffer: a contiguous CUDA tensor of exactly
+    ``shape`` and ``dtype`` on ``device`` (the kernels write every element of
+    that shape, so anything smaller would be overrun)."""
+    import torch
+
+    if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device or tuple(t.shape) != tuple(shape)
+            or t.dtype != dtype or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} CUDA tensor of shape {tuple(shape)} on {device}")
+
+
+def _check_workspace(ws, device):
+    import torch
+
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {device}")
+
+
+def _check_qkv_device(q, k, v):
+    """q, k, v: contiguous 4-D CUDA tensors of one dtype on one device, k and
+    v of one shape (B, Sk, Hkv, D) matching q's batch and head dimension."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    if not (q.dtype == k.dtype == v.dtype) or not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must share one dtype and device")
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != q.shape[0] or k.shape[3] != q.shape[3]:
+        raise ValueError("k and v must be (B, Sk, Hkv, D) matching q")
+
+
 def fa_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, return_lse=True, stream=None):
     """Attention forward: returns (O, LSE) (LSE is None if return_lse is False
     and no ``lse`` buffer is given).
@@ -222,11 +254,17 @@ def fa_merge(o_parts, lse_parts, *, out=None, lse=None, return_lse=True, stream=
         raise ValueError("lse_parts must be float32 (n, B, Hq, Sq)")
     if not (o_parts.is_cuda and lse_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()):
         raise ValueError("o_parts and lse_parts must be contiguous CUDA tensors")
+    if lse_parts.device != o_parts.device:
+        raise ValueError("o_parts and lse_parts must be on one device")
     code = _dtype_code(o_parts)
     if out is None:
         out = torch.empty((B, Sq, Hq, D), dtype=o_parts.dtype, device=o_parts.device)
+    else:
+        _check_result("out", out, (B, Sq, Hq, D), o_parts.dtype, o_parts.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=o_parts.device)
+    elif lse is not None:
+        _check_result("lse", lse, (B, Hq, Sq), torch.float32, o_parts.device)
     with torch.cuda.device(o_parts.device):
         rc = lib().fa_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, out.data_ptr(),
                             lse.data_ptr() if lse is not None else None, B, Sq, Hq, D, code,
@@ -256,15 +294,9 @@ def fa_fwd_decode(q, k, v, *, scale=None, causal=False, num_splits=0, workspace=
     """
     import torch
 
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
-    if not (q.dtype == k.dtype == v.dtype) or not (q.device == k.device == v.device):
-        raise ValueError("q, k and v must share one dtype and device")
+    _check_qkv_device(q, k, v)
     B, Sq, Hq, D = q.shape
     _, Sk, Hkv, _ = k.shape
-    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
-        raise ValueError("k and v must be (B, Sk, Hkv, D) matching q")
     code = _dtype_code(q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -272,10 +304,16 @@ def fa_fwd_decode(q, k, v, *, scale=None, causal=False, num_splits=0, workspace=
         need = fa_decode_workspace_size(B, Sq, Sk, Hq, Hkv, D, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        elif workspace is not None:
+            _check_workspace(workspace, q.device)   # its size is checked by the C call
         if out is None:
             out = torch.empty_like(q)
+        else:
+            _check_result("out", out, q.shape, q.dtype, q.device)
         if lse is None and return_lse:
             lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+        elif lse is not None:
+            _check_result("lse", lse, (B, Hq, Sq), torch.float32, q.device)
         rc = lib().fa_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                  lse.data_ptr() if lse is not None else None, B, Sq, Sk, Hq, Hkv, D, float(scale),
                                  int(bool(causal)), code, int(num_splits),
@@ -295,9 +333,7 @@ def fa_fwd_decode_noalloc(q, k, v, *, scale=None, causal=False, num_splits=0, ou
     and race; order them on one stream."""
     import torch
 
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    _check_qkv_device(q, k, v)
     B, Sq, Hq, D = q.shape
     _, Sk, Hkv, _ = k.shape
     code = _dtype_code(q)
@@ -305,8 +341,12 @@ def fa_fwd_decode_noalloc(q, k, v, *, scale=None, causal=False, num_splits=0, ou
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
+    else:
+        _check_result("out", out, q.shape, q.dtype, q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _check_result("lse", lse, (B, Hq, Sq), torch.float32, q.device)
     with torch.cuda.device(q.device):
         rc = lib().fa_fwd_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                          lse.data_ptr() if lse is not None else None, B, Sq, Sk, Hq, Hkv, D,
@@ -375,8 +415,9 @@ def fa_fwd_host(q, k, v, *, scale=None, causal=False, out=None, lse=None, return
     need = fa_fwd_host_workspace_size(B, Sq, Sk, Hq, Hkv, D)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=torch.device("cuda", dev))
-    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
-        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    elif (not workspace.is_cuda or workspace.get_device() != dev or not workspace.is_contiguous()
+          or workspace.numel() * workspace.element_size() < need):
+        raise ValueError(f"workspace must be a contiguous CUDA tensor of at least {need} bytes on cuda:{dev}")
 
     def call():
         h = _stream_handle(stream, dev)

@@ -81,3 +81,36 @@ def test_decode_rejects_small_workspace():
     small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(api.FAError):
         api.fa_fwd_decode(q, k, v, causal=True, num_splits=4, workspace=small)
+
+
+def test_binding_rejects_result_buffers_that_do_not_fit():
+    """The kernels write every element of O and LSE, so the binding refuses a
+    caller buffer of another shape, dtype or device (and a workspace in host
+    memory) before anything is launched; buffers that fit are used as given."""
+    w = W(2, 1, 1000, 16, 4, 128)
+    q, k, v = (t.cuda() for t in draw_inputs(w))
+    few_heads = torch.empty(2, 1, 8, 128, dtype=q.dtype, device="cuda")
+    with pytest.raises(ValueError):
+        api.fa_fwd_decode(q, k, v, out=few_heads)
+    with pytest.raises(ValueError):
+        api.fa_fwd_decode(q, k, v, lse=torch.empty(2, 16, 2, device="cuda"))
+    with pytest.raises(ValueError):
+        api.fa_fwd_decode(q, k, v, num_splits=4, workspace=torch.empty(1 << 20, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        api.fa_fwd_decode_noalloc(q, k, v, out=few_heads)
+    with pytest.raises(ValueError):
+        api.fa_fwd_decode_noalloc(q, k, v, lse=torch.empty(2, 16, 1, dtype=torch.float16, device="cuda"))
+    with pytest.raises(ValueError):
+        api.fa_fwd_decode_noalloc(q, k[:, :, :2].contiguous(), v)
+    parts_o = torch.zeros(3, 2, 1, 16, 128, dtype=q.dtype, device="cuda")
+    parts_l = torch.zeros(3, 2, 16, 1, device="cuda")
+    with pytest.raises(ValueError):
+        api.fa_merge(parts_o, parts_l, out=few_heads)
+    with pytest.raises(ValueError):
+        api.fa_merge(parts_o, parts_l, lse=torch.empty(2, 16, 1, dtype=torch.float64, device="cuda"))
+    out = torch.empty_like(q)
+    lse = torch.empty(2, 16, 1, device="cuda")
+    o, l = api.fa_merge(parts_o, parts_l, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert o is out and l is lse
+    assert torch.all(out == 0) and torch.allclose(lse, torch.full_like(lse, float(torch.log(torch.tensor(3.0)))))
