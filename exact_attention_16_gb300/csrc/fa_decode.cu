@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -28,12 +29,18 @@ struct Plan {
   unsigned long long workspace_bytes() const { return n_splits > 1 ? o_part_bytes + lse_part_bytes : 0; }
 };
 
+// SM count of the current device, looked up once per device (calls from
+// several host threads may race to look it up; they store the same value).
 int device_sms() {
-  static int sms[kMaxDevices] = {0};
+  static std::atomic<int> sms[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  if (sms[dev] == 0) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev];
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    sms[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 // Row tiles of floor(128 / G) query positions, and splits of the key range:
