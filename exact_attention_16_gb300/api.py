@@ -33,6 +33,7 @@ __all__ = [
     "fa_debug_set_fault",
     "fa_debug_set_schedule",
     "fa_fwd_schedule",
+    "fa_fwd_work_items",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -80,6 +81,9 @@ EXPORTED_SYMBOLS = {
                     + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_ulonglong,
                        ctypes.c_void_p]),
     "fa_fwd_schedule": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)]),
+    "fa_fwd_work_items": (ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_int,
+                                                              ctypes.POINTER(ctypes.c_int),
+                                                              ctypes.POINTER(ctypes.c_int)]),
 }
 
 
@@ -460,6 +464,27 @@ def fa_fwd_schedule(B: int, Sq: int, Sk: int, Hq: int, Hkv: int, causal: bool, n
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_schedule")
     return int(out.value)
+
+
+def fa_fwd_work_items(B: int, Sq: int, Sk: int, Hq: int, Hkv: int, causal: bool, key_split: int, num_sms: int):
+    """The persistent kernel's work items for these sizes (host only): an
+    (n_items, 8) int32 array of rows (b, hq0, hq1, kvh, r0, r1, n_kv, cta),
+    and the CTA count."""
+    import numpy as np
+
+    n = ctypes.c_int(0)
+    g = ctypes.c_int(0)
+    rc = lib().fa_fwd_work_items(int(B), int(Sq), int(Sk), int(Hq), int(Hkv), int(causal), int(key_split),
+                                 int(num_sms), None, 0, ctypes.byref(n), ctypes.byref(g))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_work_items")
+    items = np.zeros((n.value, 8), dtype=np.int32)
+    rc = lib().fa_fwd_work_items(int(B), int(Sq), int(Sk), int(Hq), int(Hkv), int(causal), int(key_split),
+                                 int(num_sms), items.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n),
+                                 ctypes.byref(g))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_work_items")
+    return items, int(g.value)
 
 
 def fa_debug_set_schedule(mode: int) -> int:

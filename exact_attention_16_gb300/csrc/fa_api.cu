@@ -377,6 +377,49 @@ extern "C" int fa_fwd_schedule(int B, int Sq, int Sk, int Hq, int Hkv, int causa
   return FA_OK;
 }
 
+extern "C" int fa_fwd_work_items(int B, int Sq, int Sk, int Hq, int Hkv, int causal, int key_split, int num_sms,
+                                 int* items, int cap, int* n_items, int* grid) {
+  if (!n_items || !grid || (cap > 0 && !items) || cap < 0 || B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0 ||
+      Hq % Hkv != 0 || num_sms <= 0 || (causal != 0 && causal != 1) || (key_split != 0 && key_split != 1))
+    return FA_ERR_INVALID_ARG;
+  fa::FwdParams p{};
+  p.B = B;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = Hq / Hkv;
+  p.causal = causal;
+  p.n_mtiles = (Sq + fa::kBM - 1) / fa::kBM;
+  p.n_kv_tiles = (Sk + fa::kBN - 1) / fa::kBN;
+  if (static_cast<long long>(B) * Hq * p.n_mtiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  set_items(p, key_split == 1);
+  p.n_items = static_cast<int>(static_cast<long long>(B) * p.n_units * p.n_mslots);
+  const int g = std::min(p.n_items, num_sms);
+  *n_items = p.n_items;
+  *grid = g;
+  const int n = std::min(p.n_items, cap);
+  for (int idx = 0; idx < n; ++idx) {
+    const fa::WorkItem w = key_split ? fa::decode_item<true>(p, idx) : fa::decode_item<false>(p, idx);
+    int* it = items + 8LL * idx;
+    it[0] = w.b;
+    it[1] = w.hq0;
+    it[2] = w.hq1;
+    it[3] = w.kvh;
+    it[4] = w.r0;
+    it[5] = w.r1;
+    it[6] = w.n_kv;
+    it[7] = -1;
+  }
+  // the CTA that runs each item: the kernel's loop over rounds
+  for (int round = 0; static_cast<long long>(round) * g < p.n_items; ++round)
+    for (int cta = 0; cta < g; ++cta) {
+      const int idx = fa::item_of_round(round, cta, g);
+      if (idx < n) items[8LL * idx + 7] = cta;
+    }
+  return FA_OK;
+}
+
 extern "C" int fa_debug_set_schedule(int mode) {
   if (mode < -1 || mode > 1) return FA_ERR_INVALID_ARG;
   g_schedule_mode.store(mode);

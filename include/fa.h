@@ -258,6 +258,31 @@ int fa_debug_set_fault(int skip_load, int timeout_ms);
 int fa_fwd_schedule(int B, int Sq, int Sk, int Hq, int Hkv, int causal, int num_sms, int* key_split);
 
 /*
+ * fa_fwd_work_items — the work items of fa_fwd's persistent kernel for these
+ * sizes (head dimension <= 128) under one decomposition (key_split 0:
+ * row-tile pairs, 1: key-split items), from the functions the kernel itself
+ * runs, without touching any GPU. Items are numbered longest first (row
+ * tiles from the last down, then batch, then head unit) and run by CTA
+ * r * grid + c on even rounds r and r * grid + (grid - 1 - c) on odd ones
+ * ("NVIDIA闪存注意力实操" section "ProgramId重映射": longest work first).
+ * For item n < min(*n_items, cap) it writes eight ints at items[8 n]:
+ *   b, hq0, hq1  batch and the query heads of its two 128-row tiles,
+ *   kvh          their key/value head (hq / (Hq / Hkv), "MiniPaged-Qwen"
+ *                section 6),
+ *   r0, r1       first rows of the two tiles (a key-split item has one tile:
+ *                hq1 = hq0, r1 = r0; a tile with r >= Sq is empty),
+ *   n_kv         key tiles [0, n_kv) the item visits (the causal limit of
+ *                its last row, "MiniPaged-Qwen" section 13; 0: no key),
+ *   cta          the CTA that runs it.
+ * *n_items is the full item count and *grid the CTA count (at most
+ * num_sms). `items` is caller memory of at least 8 * cap ints (may be NULL
+ * when cap is 0). FA_ERR_INVALID_ARG for null outputs, non-positive sizes,
+ * Hq not a multiple of Hkv, or causal / key_split outside {0, 1}.
+ */
+int fa_fwd_work_items(int B, int Sq, int Sk, int Hq, int Hkv, int causal, int key_split, int num_sms, int* items,
+                      int cap, int* n_items, int* grid);
+
+/*
  * fa_debug_set_schedule — test hook that fixes the work decomposition of
  * every later fa_fwd / fa_fwd_strided call in this process (D <= 128):
  *   -1  (default) a host cost model picks per call;
