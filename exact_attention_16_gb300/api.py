@@ -26,6 +26,7 @@ __all__ = [
     "fa_fwd_decode_noalloc",
     "fa_fwd_host",
     "fa_fwd_host_workspace_size",
+    "fa_fwd_host_plan",
     "fa_decode_splits",
     "fa_status",
     "fa_status_string",
@@ -84,6 +85,8 @@ EXPORTED_SYMBOLS = {
     "fa_fwd_work_items": (ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_int,
                                                               ctypes.POINTER(ctypes.c_int),
                                                               ctypes.POINTER(ctypes.c_int)]),
+    "fa_fwd_host_plan": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_int,
+                                                             ctypes.POINTER(ctypes.c_int)]),
 }
 
 
@@ -436,6 +439,23 @@ def fa_fwd_host(q, k, v, *, scale=None, causal=False, out=None, lse=None, return
 
     _call_on(dev, call)
     return out, lse
+
+
+def fa_fwd_host_plan(B, Sq, Sk, Hq, Hkv, D, causal):
+    """fa_fwd_host's chunks for these sizes (host only): an (n, 9) int32 array
+    of rows (b0, b1, h0, h1, r0, r1, k0, k1, lim)."""
+    import numpy as np
+
+    n = ctypes.c_int(0)
+    args = (int(B), int(Sq), int(Sk), int(Hq), int(Hkv), int(D), int(causal))
+    rc = lib().fa_fwd_host_plan(*args, None, 0, ctypes.byref(n))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_host_plan")
+    out = np.zeros((n.value, 9), dtype=np.int32)
+    rc = lib().fa_fwd_host_plan(*args, out.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_host_plan")
+    return out
 
 
 def fa_status(stream=None) -> int:

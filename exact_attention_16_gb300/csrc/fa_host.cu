@@ -161,6 +161,24 @@ extern "C" int fa_fwd_host_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv
   return FA_OK;
 }
 
+extern "C" int fa_fwd_host_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int causal, int* chunks, int cap,
+                                int* n_chunks) {
+  if (!n_chunks || (cap > 0 && !chunks) || cap < 0 || B <= 0 || Sq <= 0 || Sk < 0 || Hq <= 0 || Hkv <= 0 ||
+      Hq % Hkv != 0 || D <= 0 || (causal != 0 && causal != 1))
+    return FA_ERR_INVALID_ARG;
+  Layout l;
+  layout_of(B, Sq, Sk, Hq, Hkv, D, &l);
+  Chunk ch[kMaxChunks];
+  const int n = plan_chunks(B, Sq, Sk, Hkv, causal, l.q_bytes + 2 * l.kv_bytes + l.o_bytes + l.lse_bytes, ch);
+  *n_chunks = n;
+  for (int i = 0; i < n && i < cap; ++i) {
+    const Chunk& x = ch[i];
+    const int v[9] = {x.b0, x.b1, x.h0, x.h1, x.r0, x.r1, x.k0, x.k1, x.lim};
+    for (int j = 0; j < 9; ++j) chunks[9 * i + j] = v[j];
+  }
+  return FA_OK;
+}
+
 extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Sk,
                            int Hq, int Hkv, int D, float scale, int causal, int dtype, void* workspace,
                            unsigned long long workspace_bytes, fa_stream_t stream_) {

@@ -222,6 +222,21 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
                 unsigned long long workspace_bytes, fa_stream_t stream);
 
 /*
+ * fa_fwd_host_plan — the chunks fa_fwd_host cuts these sizes into, without
+ * touching any GPU (host arithmetic only). For chunk i < min(*n_chunks, cap)
+ * it writes nine ints at chunks[9 i]: batches [b0, b1), KV heads [h0, h1)
+ * (query heads [h0 G, h1 G), G = Hq / Hkv), query rows [r0, r1), the keys
+ * [k0, k1) the chunk copies in (those its rows need that no earlier chunk of
+ * the same heads copied), and lim: its kernel runs on keys [0, lim) with the
+ * bottom-right mask, which for rows [r0, r1) is the mask of the whole
+ * problem. *n_chunks is the chunk count (1 to 8). `chunks` is caller memory
+ * of at least 9 * cap ints (may be NULL when cap is 0). FA_ERR_INVALID_ARG
+ * for a null `n_chunks`, non-positive B, Sq, Hq, Hkv or D, a negative Sk, Hq
+ * not a multiple of Hkv, or causal outside {0, 1}.
+ */
+int fa_fwd_host_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int causal, int* chunks, int cap, int* n_chunks);
+
+/*
  * fa_status — synchronise `stream`, then read and clear the device status
  * word of the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel's bounded
  * wait on an mbarrier ran out (the kernel then released its tensor memory
