@@ -6,7 +6,8 @@ tile's max exceeds it by more than 8 (log2 units), weights p = 2^(s c - m)
 in fp32 with c = scale * log2(e), P rounded to bf16 (round to nearest even)
 for the P V product, the row sum l taken over the unrounded fp32 p, and the
 rounding error of each tile's largest P added to a correction term l_corr
-that only the O normalisation uses (O = O~ / (l + l_corr); LSE from l).
+that only the O normalisation uses (O = O~ / (l + l_corr); LSE from l);
+and, for key-split items, the combine of the two slots' partial states.
 It is a model of the design, not of the compiled code: it shows that the
 tolerance the GPU tests apply (O max-abs 2e-2, mean-abs 2e-3, LSE 1e-3)
 holds for this arithmetic with margin, and why the correction term is there:
@@ -34,9 +35,9 @@ def bf16_round(x):
     return r.view(np.float32)
 
 
-def model_head(q, k, v, scale, causal, use_corr=True):
-    """One (batch, head): q (Sq, D), k, v (Sk, D) float32 holding bf16 values.
-    Returns O (Sq, D) as bf16 values and LSE (Sq,) in float32."""
+def slot_state(q, k, v, scale, causal, tiles):
+    """Running (m, l, l_corr, O~) of one row tile over the key tiles `tiles`
+    (in order), as one kernel slot keeps them."""
     Sq, Sk = q.shape[0], k.shape[0]
     c = np.float32(scale * math.log2(math.e))
     m = np.full(Sq, -np.inf, dtype=np.float32)
@@ -44,17 +45,17 @@ def model_head(q, k, v, scale, causal, use_corr=True):
     l_corr = np.zeros(Sq, dtype=np.float32)
     acc = np.zeros((Sq, q.shape[1]), dtype=np.float32)
     rows = np.arange(Sq)[:, None]
-    for j0 in range(0, Sk, 128):
+    for j0 in (128 * t for t in tiles):
         kt, vt = k[j0:j0 + 128], v[j0:j0 + 128]
         s = (q.astype(np.float64) @ kt.T.astype(np.float64)).astype(np.float32)   # fp32 accumulation
         cols = j0 + np.arange(kt.shape[0])[None, :]
         if causal:
             s = np.where(cols <= rows + (Sk - Sq), s, np.float32(-np.inf))
         mx = s.max(axis=1)
-        with np.errstate(invalid="ignore"):
+        with np.errstate(invalid="ignore"):     # rows with no visible key yet: -inf - -inf
             m_new = np.maximum(m, (mx * c).astype(np.float32))
             move = m_new > m + np.float32(THRESHOLD)
-        alpha = np.where(move, np.exp2((m - m_new).astype(np.float32)), np.float32(1.0)).astype(np.float32)
+            alpha = np.where(move, np.exp2((m - m_new).astype(np.float32)), np.float32(1.0)).astype(np.float32)
         alpha = np.where(np.isneginf(m) & move, np.float32(0.0), alpha)
         m = np.where(move, m_new, m)
         l, l_corr = (l * alpha).astype(np.float32), (l_corr * alpha).astype(np.float32)
@@ -70,6 +71,29 @@ def model_head(q, k, v, scale, causal, use_corr=True):
         l_corr = (l_corr + (bf16_round(pmax) - pmax)).astype(np.float32)
         l = (l + p.sum(axis=1, dtype=np.float32)).astype(np.float32)
         acc = (acc + (pb.astype(np.float64) @ vt.astype(np.float64)).astype(np.float32)).astype(np.float32)
+    return m, l, l_corr, acc
+
+
+def model_head(q, k, v, scale, causal, use_corr=True, key_split=False):
+    """One (batch, head): q (Sq, D), k, v (Sk, D) float32 holding bf16 values.
+    Returns O (Sq, D) as bf16 values and LSE (Sq,) in float32. With
+    `key_split` two slots take the even and the odd key tiles and are
+    combined before the store: a_t = 2^(m_t - max(m_0, m_1)),
+    O = (a_0 O~_0 + a_1 O~_1) / (a_0 (l_0 + c_0) + a_1 (l_1 + c_1)), LSE from
+    a_0 l_0 + a_1 l_1."""
+    n_tiles = (k.shape[0] + 127) // 128
+    if not key_split:
+        m, l, l_corr, acc = slot_state(q, k, v, scale, causal, range(n_tiles))
+    else:
+        m0, l0, c0, o0 = slot_state(q, k, v, scale, causal, range(0, n_tiles, 2))
+        m1, l1, c1, o1 = slot_state(q, k, v, scale, causal, range(1, n_tiles, 2))
+        m = np.maximum(m0, m1)
+        with np.errstate(invalid="ignore"):
+            a0 = np.where(np.isneginf(m0), np.float32(0.0), np.exp2(m0 - m)).astype(np.float32)
+            a1 = np.where(np.isneginf(m1), np.float32(0.0), np.exp2(m1 - m)).astype(np.float32)
+        l = (a0 * l0 + a1 * l1).astype(np.float32)
+        l_corr = (a0 * c0 + a1 * c1).astype(np.float32)
+        acc = (a0[:, None] * o0 + a1[:, None] * o1).astype(np.float32)
     live = l > 0
     denom = (l + l_corr) if use_corr else l
     o = np.where(live[:, None], acc / np.where(live, denom, 1.0)[:, None], 0.0).astype(np.float32)
@@ -77,7 +101,7 @@ def model_head(q, k, v, scale, causal, use_corr=True):
     return bf16_round(o), lse.astype(np.float32)
 
 
-def model(q, k, v, scale, causal, use_corr=True):
+def model(q, k, v, scale, causal, use_corr=True, key_split=False):
     B, Sq, Hq, D = q.shape
     G = Hq // k.shape[2]
     o = np.zeros((B, Sq, Hq, D), dtype=np.float32)
@@ -85,7 +109,7 @@ def model(q, k, v, scale, causal, use_corr=True):
     for b in range(B):
         for h in range(Hq):
             o[b, :, h], lse[b, h] = model_head(q[b, :, h], k[b, :, h // G], v[b, :, h // G], scale, causal,
-                                               use_corr)
+                                               use_corr, key_split)
     return o, lse
 
 
@@ -116,11 +140,12 @@ def test_bf16_round_is_nearest_even():
     assert abs(got[4] - want[4]) <= 2 ** -9 * 2.5e-3           # within half a bf16 ulp
 
 
+@pytest.mark.parametrize("key_split", [False, True], ids=["one_slot", "key_split"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_model_of_the_kernel_arithmetic_is_within_the_tolerance(w):
+def test_model_of_the_kernel_arithmetic_is_within_the_tolerance(w, key_split):
     q, k, v = _inputs(w)
     o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
-    o, lse = model(q, k, v, w.scale, w.causal)
+    o, lse = model(q, k, v, w.scale, w.causal, key_split=key_split)
     o_max, o_mean, lse_max = _errors(o, lse, o_ref, lse_ref)
     assert o_max <= O_MAX_ABS * 0.75, o_max                  # a quarter of the bound to spare
     assert o_mean <= O_MEAN_ABS * 0.5, o_mean
