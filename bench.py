@@ -38,6 +38,7 @@ from exact_attention_16_gb300.workloads import WORKLOADS, by_name, draw_inputs  
 
 DEFAULT_WORKLOAD = "causal_gqa8_b1_s16384"
 L2_BYTES = 129 * 1000 * 1000
+DATASHEET_BF16_TFLOPS = 2250.0   # GB300 dense BF16/FP16 tensor peak (nominal, without 2:4 sparsity)
 METRIC = "attention fwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 tensor peak"
 KERNEL_SOURCES = ["exact_attention_16_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_16_gb300/csrc/ptx_sm103.cuh"]
 TRAFFIC_SUMMARY = "profiles/fa_fwd_kernel_traffic.md"
@@ -296,6 +297,8 @@ def run_ours(args, w):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "pct_of_peak": round(100.0 * (value / world) / peaks["bf16_tflops"], 2),
+        "pct_of_peak_source": peaks["source"] + " bf16 burst (cuBLAS)",
+        "pct_of_datasheet_peak": round(100.0 * (value / world) / DATASHEET_BF16_TFLOPS, 2),
         "roofline": {
             "bound": "tensor",
             "achieved": round(achieved, 2),
@@ -305,7 +308,7 @@ def run_ours(args, w):
             "peak_source": peaks["source"] + " bf16 burst",
             "traffic": recorded_traffic(w.name),
             "algorithmic_bytes": metrics.algorithmic_bytes(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D),
-            "kernel": "fa_fwd_kernel",
+            "kernel": "fa_fwd_kernel" if w.D <= 128 else "fa_decode_kernel",
             "avg_launch_ms": round(avg_launch_ms, 4),
         },
         "exp_roofline": exp_roofline(flop, w.D, avg_launch_ms),

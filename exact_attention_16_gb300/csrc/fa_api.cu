@@ -226,7 +226,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (B < 0 || Sq < 0 || Sk < 0 || Hq < 0 || Hkv < 0 || D < 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  // any finite scale, as long as scale * log2(e) is a finite float
+  if (std::fabs(static_cast<double>(scale)) * 1.4426950408889634 > 3.4028234663852886e38)
+    return FA_ERR_UNSUPPORTED;
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
   if (D < 16 || D > 256 || D % 16 != 0) return FA_ERR_UNSUPPORTED;
@@ -280,7 +283,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.Hkv = Hkv;
   p.group = Hq / Hkv;
   p.causal = causal;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // A zero scale makes every visible score 0: it runs as scale 1 on Q read as
+  // zeros (the same scores, exactly), so that the kernels always have a
+  // nonzero scale to rank scores by.
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale == 0.0f ? 1.0f : scale) * 1.4426950408889634);
+  p.q_b_shift = scale == 0.0f ? B : 0;
   p.n_mtiles = (Sq + fa::kBM - 1) / fa::kBM;
   p.n_kv_tiles = (Sk + fa::kBN - 1) / fa::kBN;
   // every item count below fits an int: B * Hq * ceil(Sq / 128) does

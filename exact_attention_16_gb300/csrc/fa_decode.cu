@@ -149,7 +149,11 @@ int decode_launch(const void* q, const void* k, const void* v, void* o, float* l
   p.P = pl.positions;
   p.n_row_tiles = pl.n_row_tiles;
   p.causal = causal;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // A zero scale makes every visible score 0: it runs as scale 1 on Q read as
+  // zeros (the same scores, exactly), so that the kernels always have a
+  // nonzero scale to rank scores by.
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale == 0.0f ? 1.0f : scale) * 1.4426950408889634);
+  p.q_b_shift = scale == 0.0f ? B : 0;
   p.n_splits = pl.n_splits;
   p.n_kv_tiles = pl.n_tiles;
   {
@@ -209,7 +213,10 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
   int rc = check_args(B, Sq, Sk, Hq, Hkv, D, dtype);
   if (rc != FA_OK) return rc;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  // any finite scale, as long as scale * log2(e) is a finite float
+  if (std::fabs(static_cast<double>(scale)) * 1.4426950408889634 > 3.4028234663852886e38)
+    return FA_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
   if (Sk == 0) return fa_fwd(q, k, v, o, lse, B, Sq, 0, Hq, Hkv, D, scale, causal, dtype, stream_);
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;

@@ -22,6 +22,7 @@
 #include <cuda.h>
 
 #include "ptx_sm103.cuh"
+#include "softmax_row.cuh"
 
 namespace fa {
 
@@ -36,7 +37,9 @@ struct DecodeParams {
   int P;               // query positions per row tile: floor(128 / G)
   int n_row_tiles;     // ceil(Sq / P)
   int causal;
-  float scale_log2;
+  float scale_log2;    // softmax scale * log2(e); nonzero (see q_b_shift)
+  int q_b_shift;       // added to the batch coordinate of the Q load: B reads Q as
+                       // zeros (TMA zero fill), how a zero scale runs
   int n_splits, n_kv_tiles;
   int unit_group;      // (split, KV head, batch) units whose CTAs run interleaved
   unsigned long long timeout_ns;
@@ -194,7 +197,7 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ptx::mbar_arrive_expect_tx(bar_q_full, q_bytes);
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
-        ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, pos0, b, pol_q);
+        ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, pos0, b + p.q_b_shift, pol_q);
       // units in order K_0, V_0, K_1, V_1, ... (each in kHalves pieces)
       for (int u = 0; ok && u < 2 * kHalves * n; ++u) {
         const uint32_t st = u % kStages, ph = ((u / kStages) & 1u) ^ 1u;
@@ -321,20 +324,13 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       uint32_t sr[128];
       ptx::tmem_ld_32x32b_x128(tS, sr);
       float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+      // Mask where some row of the warp has hidden keys in this tile (the
+      // Sk tail, the causal limit); mx * sl2 is the row's largest scaled
+      // score and the exponents below are s * sl2 - m.
       const int lim = lim_abs - (t_begin + j) * 128;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? __uint_as_float(sr[c]) : kNegInf;
-      float mq[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) mq[c] = s[c];
-#pragma unroll
-      for (int c = 8; c < 120; c += 16) {   // columns 8 .. 119
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mq[q] = ptx::max3(mq[q], s[c + 2 * q], s[c + 2 * q + 1]);
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mq[q] = fmaxf(mq[q], s[120 + q]);   // columns 120 .. 127
-      const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
+      const float mx = prepare_row(s, __any_sync(0xffffffffu, lim < 128), lim, sl2);
       const float m_new = fmaxf(m_ref, mx * sl2);
       float alpha = 1.0f;
       const bool need = m_new > m_ref + kRescale;

@@ -20,19 +20,24 @@ constexpr unsigned long long kScratchBytes = 16ull << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
+std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
-cudaError_t g_scratch_err[kMaxDevices] = {cudaSuccess};
 
 // Device address of g_decode_scratch on the current device. In host code the
 // array's name only stands for the symbol; the address a kernel may use has
 // to come from the runtime, once per device, with that device current.
+// The library is built without relocatable device code, so the array sits in
+// a module of its own; CUDA loads modules lazily by default, and the first
+// lookup on a device is what loads it (and reserves the array's bytes). Only
+// a successful lookup is kept: a failed one (for example out of memory while
+// the module loads) is tried again on the next call.
 void* scratch_address(int dev) {
-  std::call_once(g_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_addr[dev]) {
     void* ptr = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&ptr, g_decode_scratch);
-    g_scratch_addr[dev] = g_scratch_err[dev] == cudaSuccess ? ptr : nullptr;
-  });
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess) g_scratch_addr[dev] = ptr;
+    else (void)cudaGetLastError();   // reset the runtime's last-error state for later calls
+  }
   return g_scratch_addr[dev];
 }
 

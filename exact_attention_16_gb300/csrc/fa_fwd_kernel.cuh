@@ -37,6 +37,7 @@
 #include <cuda.h>
 
 #include "ptx_sm103.cuh"
+#include "softmax_row.cuh"
 
 namespace fa {
 
@@ -56,7 +57,10 @@ struct FwdParams {
   float* lse;            // (B, Hq, Sq) fp32 natural log, contiguous, may be null
   int B, Sq, Sk, Hq, Hkv, group;
   int causal;
-  float scale_log2;      // softmax scale * log2(e)
+  float scale_log2;      // softmax scale * log2(e); nonzero (see q_b_shift)
+  int q_b_shift;         // added to the batch coordinate of every Q load: B reads
+                         // Q as zeros (out of range, TMA zero fill), which is how
+                         // a zero scale runs: 0 * q.k = 1 * (0 . k)
   int n_mtiles;          // ceil(Sq / 128)
   int pair_heads;        // 1: item = heads (2u, 2u+1) at one row tile
   int n_units;           // head units per batch entry
@@ -290,7 +294,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           ptx::tma_load_4d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tm_q, bar_q_full + 8 * t, c * 64, hq, r0,
-                           b, pol_q);
+                           b + p.q_b_shift, pol_q);
       }
       __syncwarp();
       return true;
@@ -314,7 +318,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // that its TMA load at the item boundary hits L2.
       if (ok && lane == 0) {
         const int nidx = item_of_round(round + 1, cta, grid);
-        if ((round + 1) * grid < p.n_items && nidx < p.n_items) {
+        if ((round + 1) * grid < p.n_items && nidx < p.n_items && p.q_b_shift == 0) {
           const WorkItem nw = decode_item<KSPLIT>(p, nidx);
           if (nw.n_kv > 0) {
 #pragma unroll
@@ -599,21 +603,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        if (j >= first_masked) {
-          const int lim = lim_abs - j * kBN;
-#pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -__int_as_float(0x7f800000);
-        }
-        // row max: eight independent chains of three-input max
-        float mq[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mq[q] = fmaxf(s[2 * q], s[2 * q + 1]);   // columns 0 .. 15
-#pragma unroll
-        for (int c = 16; c < 128; c += 16) {   // columns 16 .. 127
-#pragma unroll
-          for (int q = 0; q < 8; ++q) mq[q] = ptx::max3(mq[q], s[c + 2 * q], s[c + 2 * q + 1]);
-        }
-        const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
+        // Mask (only tiles from first_masked on) and the row's largest scaled
+        // score mx * sl2; the exponents below are s * sl2 - m.
+        const float mx = prepare_row(s, j >= first_masked, lim_abs - j * kBN, sl2);
         const float m_new = fmaxf(m_ref, mx * sl2);
         float alpha = 1.0f;
         const bool need = m_new > m_ref + kRescaleThreshold;

@@ -58,7 +58,10 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype_t;
  *      effect on the result, extra arithmetic). D > 128 runs the one-tile
  *      kernel of fa_fwd_decode with a single key range (no workspace) and
  *      needs Hq / Hkv <= 128.
- * scale  softmax scale (1/sqrt(D) in the usual case); finite and > 0.
+ * scale  softmax scale (1/sqrt(D) in the usual case): any finite value,
+ *      zero and negative ones included (the pages leave it a free
+ *      argument of softmax(scale * Q K^T + M)); |scale| * log2(e) must be
+ *      a finite float (|scale| < 2.36e38).
  * causal 0: every key is visible; 1: bottom-right causal mask, query i sees
  *      key j iff j <= i + Sk - Sq (top-left when Sq == Sk).
  * dtype  FA_DTYPE_FP16 or FA_DTYPE_BF16 (inputs and O share it; P is rounded
@@ -69,10 +72,11 @@ typedef enum { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype_t;
  * read. The library keeps a per-device status word and no other state.
  * Alignment: q, k, v, o must be 16-byte aligned; lse 4-byte aligned.
  * Errors: arguments are checked before anything is enqueued. Negative sizes,
- * NULL pointers, Hkv == 0 or Hq % Hkv != 0, a non-finite or non-positive
- * scale, causal not in {0,1}, dtype not in {0,1} or a misaligned pointer give
- * FA_ERR_INVALID_ARG; D outside 16..256 or not a multiple of 16, or sizes whose element offsets do not
- * fit the kernel's 32-bit tile coordinates give FA_ERR_UNSUPPORTED. With
+ * NULL pointers, Hkv == 0 or Hq % Hkv != 0, a non-finite scale, causal not
+ * in {0,1}, dtype not in {0,1} or a misaligned pointer give
+ * FA_ERR_INVALID_ARG; D outside 16..256 or not a multiple of 16, a scale
+ * whose |scale| * log2(e) overflows a float, or sizes whose element offsets
+ * do not fit the kernel's 32-bit tile coordinates give FA_ERR_UNSUPPORTED. With
  * B, Sq or Hq equal to 0 nothing is written and FA_OK is returned. Sk == 0 is
  * valid: O = 0 and LSE = -inf. A failed launch returns FA_ERR_CUDA. The call
  * is asynchronous; a device-side timeout is reported later by fa_status().
@@ -172,7 +176,15 @@ int fa_decode_splits(int B, int Sq, int Sk, int Hq, int Hkv, int D, int num_spli
  * or fa_fwd_decode with a workspace serves those sizes. The call allocates
  * nothing (no cudaMalloc/cudaFree). The first call on a device looks up the
  * array's device address on that device (once per device, with the device
- * current); make that first call before any stream capture. Every call on a
+ * current). The array sits in a device-code module of its own (the library
+ * has no relocatable device code), and under CUDA's default lazy module
+ * loading that first lookup is what loads the module and reserves its
+ * 16 MiB. A caller whose device heap is later handed to another memory
+ * manager, or who captures streams, should therefore make one call on each
+ * device at start-up, before either; setting CUDA_MODULE_LOADING=EAGER
+ * instead loads the module, array included, when the library loads. If that
+ * first lookup fails (for example no memory left for the module) the call
+ * returns FA_ERR_CUDA and the next call tries again. Every call on a
  * device shares the one array, so calls that overlap on the GPU (different
  * streams, or host threads without ordering) race on it; order them on one
  * stream. Arguments, results and errors are otherwise those of fa_fwd_decode.

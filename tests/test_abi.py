@@ -64,8 +64,11 @@ def _call(lib, **kw):
     (dict(causal=2), api.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), api.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), api.FA_ERR_INVALID_ARG),
-    (dict(scale=0.0), api.FA_ERR_INVALID_ARG),
-    (dict(scale=-0.5), api.FA_ERR_INVALID_ARG),
+    (dict(scale=3.0e38), api.FA_ERR_UNSUPPORTED),   # scale * log2(e) is not a finite float
+    (dict(scale=-3.0e38), api.FA_ERR_UNSUPPORTED),
+    (dict(scale=0.0, B=0), api.FA_OK),          # any finite scale passes the checks (B = 0: no launch)
+    (dict(scale=-0.5, B=0), api.FA_OK),
+    (dict(scale=-2.0e38, B=0), api.FA_OK),
     (dict(q=None), api.FA_ERR_INVALID_ARG),
     (dict(o=None), api.FA_ERR_INVALID_ARG),
     (dict(k=None), api.FA_ERR_INVALID_ARG),
@@ -172,7 +175,10 @@ def test_decode_rejects_before_any_launch(lib):
                                        kw.get("causal", 0), kw.get("dtype", 1), 0, None, 0, None)
     assert c(dtype=5) == api.FA_ERR_INVALID_ARG
     assert c(causal=3) == api.FA_ERR_INVALID_ARG
-    assert c(scale=0.0) == api.FA_ERR_INVALID_ARG
+    assert c(scale=float("nan")) == api.FA_ERR_INVALID_ARG
+    assert c(scale=3.0e38) == api.FA_ERR_UNSUPPORTED
+    assert c(scale=0.0, B=0) == api.FA_OK          # zero and negative scales are valid
+    assert c(scale=-1.0, B=0) == api.FA_OK
     assert c(Hq=258, Hkv=2) == api.FA_ERR_UNSUPPORTED
     assert c(B=0) == api.FA_OK
 

@@ -132,6 +132,55 @@ def test_zero_scores_give_prefix_means(Sq, Sk, causal):
             assert abs(lse[0, hq, i] - math.log(cnt)) < 1e-12
 
 
+@pytest.mark.parametrize("Sq,Sk,causal", SHAPES)
+def test_zero_scale_gives_prefix_means(Sq, Sk, causal):
+    """scale = 0 with random q: every visible score is 0 whatever q and k
+    are, so the rows are the same prefix means as for q = 0 and LSE_i =
+    ln(#visible) (the scale is a free argument of softmax(scale Q K^T + M))."""
+    B, Hq, Hkv, D = 1, 2, 1, 5
+    q, k, v = rand_qkv(13, B, Sq, Sk, Hq, Hkv, D, sigma=3.0)
+    o, lse = oracle.attention(q, k, v, 0.0, causal)
+    csum = np.cumsum(v, axis=1)
+    for hq in range(Hq):
+        for i in range(Sq):
+            cnt = n_visible(i, Sq, Sk, causal)
+            if cnt == 0:
+                assert lse[0, hq, i] == -np.inf and np.all(o[0, i, hq] == 0.0)
+                continue
+            np.testing.assert_allclose(o[0, i, hq], csum[0, cnt - 1, 0] / cnt, atol=1e-12)
+            assert abs(lse[0, hq, i] - math.log(cnt)) < 1e-12
+
+
+@pytest.mark.parametrize("Sq,Sk,causal", SHAPES)
+def test_negative_scale_equals_negated_queries(Sq, Sk, causal):
+    """scale * (q . k) = (-scale) * ((-q) . k): a negative scale gives the
+    result of its magnitude on negated queries (negation is exact in fp64)."""
+    q, k, v = rand_qkv(14, 2, Sq, Sk, 4, 2, 6)
+    o1, l1 = oracle.attention(q, k, v, -0.7, causal)
+    o2, l2 = oracle.attention(-q, k, v, 0.7, causal)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    live = np.isfinite(l2)
+    assert np.array_equal(live, np.isfinite(l1))
+    np.testing.assert_allclose(l1[live], l2[live], rtol=0, atol=1e-12)
+
+
+def test_negative_scale_two_keys_favour_the_lower_score():
+    """With a negative scale the key with the LOWER dot product gets the
+    larger weight: two keys give sigmoid weights of scale * (a - b)."""
+    rng = np.random.default_rng(15)
+    q = rng.standard_normal((1, 5, 1, 4))
+    k = rng.standard_normal((1, 2, 1, 4))
+    v = rng.standard_normal((1, 2, 1, 4))
+    scale = -1.3
+    o, lse = oracle.attention(q, k, v, scale, causal=False)
+    for i in range(5):
+        a = float(np.dot(q[0, i, 0], k[0, 0, 0]))
+        b = float(np.dot(q[0, i, 0], k[0, 1, 0]))
+        w0 = sps.expit(scale * (a - b))
+        np.testing.assert_allclose(o[0, i, 0], w0 * v[0, 0, 0] + (1 - w0) * v[0, 1, 0], atol=1e-13)
+        assert abs(lse[0, 0, i] - np.logaddexp(scale * a, scale * b)) < 1e-12
+
+
 def test_two_keys_weights_are_sigmoids():
     rng = np.random.default_rng(4)
     Sq, Sk, D = 6, 2, 3
