@@ -155,6 +155,17 @@ __host__ __device__ __forceinline__ int item_of_round(int round, int cta, int gr
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
+// The first round >= r in which CTA `cta` has an item with at least one key
+// tile, or -1 when it has none left.
+template <bool KSPLIT>
+__host__ __device__ __forceinline__ int next_round(const FwdParams& p, int r, int cta, int grid) {
+  for (;; ++r) {
+    if (static_cast<long long>(r) * grid >= p.n_items) return -1;
+    const int idx = item_of_round(r, cta, grid);
+    if (idx < p.n_items && decode_item<KSPLIT>(p, idx).n_kv > 0) return r;
+  }
+}
+
 // Bounded wait on an mbarrier phase. Returns false when the CTA aborted or the
 // wait ran past the time limit (which records kStatusTimeout and aborts).
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -262,24 +273,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint32_t slot_it = 0, act = 0;
     int load_idx = 0;
     bool ok = true;
-    // Fill the next slot: tile (map0, key tile j0) at position 0 and, when
-    // map1 is given, (map1, j1) at position 1.
-    auto load_slot = [&](const CUtensorMap* map0, int j0, const CUtensorMap* map1, int j1, int kvh,
-                         int b) -> bool {
+    // Fill the next slot: tile (map0, key tile j0) of (kvh0, b0) at position 0
+    // and (map1, j1) of (kvh1, b1) at position 1; either map may be null.
+    auto load_slot = [&](const CUtensorMap* map0, int j0, int kvh0, int b0, const CUtensorMap* map1, int j1,
+                         int kvh1, int b1) -> bool {
       const uint32_t sl = slot_it % kSlots;
       const uint32_t ph = ((slot_it / kSlots) & 1u) ^ 1u;
       if (!bar_wait(bar_kv_empty + 8 * sl, ph, abort_flag, p)) return false;
       if (lane == 0 && load_idx != p.inject_skip_load) {
-        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * sl, (map1 ? 2 : 1) * L::kTileBytes);
+        ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * sl, ((map0 ? 1 : 0) + (map1 ? 1 : 0)) * L::kTileBytes);
         const uint32_t dst = sKV + sl * 2 * L::kTileBytes;
+        if (map0) {
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_4d(dst + c * L::kChunkBytes, map0, bar_kv_full + 8 * sl, c * 64, kvh, j0 * kBN, b, pol_kv);
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_4d(dst + c * L::kChunkBytes, map0, bar_kv_full + 8 * sl, c * 64, kvh0, j0 * kBN, b0,
+                             pol_kv);
+        }
         if (map1) {
 #pragma unroll
           for (int c = 0; c < L::kChunks; ++c)
-            ptx::tma_load_4d(dst + L::kTileBytes + c * L::kChunkBytes, map1, bar_kv_full + 8 * sl, c * 64, kvh,
-                             j1 * kBN, b, pol_kv);
+            ptx::tma_load_4d(dst + L::kTileBytes + c * L::kChunkBytes, map1, bar_kv_full + 8 * sl, c * 64, kvh1,
+                             j1 * kBN, b1, pol_kv);
         }
       }
       __syncwarp();
@@ -299,47 +313,71 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       __syncwarp();
       return true;
     };
-    for (int round = 0; ok; ++round) {
-      const int idx = item_of_round(round, cta, grid);
-      if (round * grid >= p.n_items) break;
-      if (idx >= p.n_items) continue;
-      const WorkItem w = decode_item<KSPLIT>(p, idx);
-      if (w.n_kv == 0) continue;
-      const int n = w.n_kv;
-      // key-split: slot t runs key tiles t, t+2, ...; n1 of them for slot 1
-      const int n1 = n / 2, n0 = n - n1;
-      // first slot: K_0 (and, key-split, K_1)
-      if constexpr (KSPLIT)
-        ok = load_q(0, w.hq0, w.r0, w.b) && load_slot(&tm_k, 0, n1 > 0 ? &tm_k : nullptr, 1, w.kvh, w.b);
-      else
-        ok = load_q(0, w.hq0, w.r0, w.b) && load_slot(&tm_k, 0, nullptr, 0, w.kvh, w.b) &&
-             load_q(1, w.hq1, w.r1, w.b);
-      // Q tiles are read once from HBM: pull the next item's into L2 now so
-      // that its TMA load at the item boundary hits L2.
-      if (ok && lane == 0) {
-        const int nidx = item_of_round(round + 1, cta, grid);
-        if ((round + 1) * grid < p.n_items && nidx < p.n_items && p.q_b_shift == 0) {
-          const WorkItem nw = decode_item<KSPLIT>(p, nidx);
-          if (nw.n_kv > 0) {
+    // Q tiles are read once from HBM: pull the next item's into L2 while
+    // this one runs, so that its TMA load at the item boundary hits L2.
+    auto prefetch_q = [&](const WorkItem& nw) {
+      if (lane == 0 && p.q_b_shift == 0) {
 #pragma unroll
-            for (int c = 0; c < L::kChunks; ++c) {
-              ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq0, nw.r0, nw.b);
-              if (!KSPLIT) ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq1, nw.r1, nw.b);
-            }
-          }
+        for (int c = 0; c < L::kChunks; ++c) {
+          ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq0, nw.r0, nw.b);
+          if (!KSPLIT) ptx::tma_prefetch_l2_4d(&tm_q, c * 64, nw.hq1, nw.r1, nw.b);
         }
       }
-      if constexpr (KSPLIT) {
+    };
+    if constexpr (KSPLIT) {
+      for (int round = 0; ok; ++round) {
+        const int idx = item_of_round(round, cta, grid);
+        if (round * grid >= p.n_items) break;
+        if (idx >= p.n_items) continue;
+        const WorkItem w = decode_item<KSPLIT>(p, idx);
+        if (w.n_kv == 0) continue;
+        const int n = w.n_kv;
+        // slot t runs key tiles t, t+2, ...; n1 of them for slot 1
+        const int n1 = n / 2, n0 = n - n1;
+        // first slot: K_0 and K_1
+        ok = load_q(0, w.hq0, w.r0, w.b) &&
+             load_slot(&tm_k, 0, w.kvh, w.b, n1 > 0 ? &tm_k : nullptr, 1, w.kvh, w.b);
+        const int nr = next_round<KSPLIT>(p, round + 1, cta, grid);
+        if (ok && nr >= 0) prefetch_q(decode_item<KSPLIT>(p, item_of_round(nr, cta, grid)));
         // per step s, for slot 0 then slot 1: (V of its tile, K of its next tile)
         for (int st = 0; ok && st < n0; ++st) {
-          ok = load_slot(&tm_v, 2 * st, st + 1 < n0 ? &tm_k : nullptr, 2 * st + 2, w.kvh, w.b);
-          if (ok && st < n1) ok = load_slot(&tm_v, 2 * st + 1, st + 1 < n1 ? &tm_k : nullptr, 2 * st + 3, w.kvh, w.b);
+          ok = load_slot(&tm_v, 2 * st, w.kvh, w.b, st + 1 < n0 ? &tm_k : nullptr, 2 * st + 2, w.kvh, w.b);
+          if (ok && st < n1)
+            ok = load_slot(&tm_v, 2 * st + 1, w.kvh, w.b, st + 1 < n1 ? &tm_k : nullptr, 2 * st + 3, w.kvh, w.b);
         }
-      } else {
-        for (int j = 0; ok && j < n; ++j)
-          ok = load_slot(&tm_v, j, j + 1 < n ? &tm_k : nullptr, j + 1, w.kvh, w.b);
+        ++act;
       }
-      ++act;
+    } else {
+      // Row-tile pairs: the CTA's items form one stream of slots. Slot use u
+      // holds (V_{j-1}, K_j) of one item, and an item's last slot holds its
+      // last V together with K_0 of the CTA's next item, so that the next
+      // item's first Q K^T can start as soon as this item's last P V is issued.
+      int round = next_round<KSPLIT>(p, 0, cta, grid);
+      bool first = true;
+      while (ok && round >= 0) {
+        const WorkItem w = decode_item<KSPLIT>(p, item_of_round(round, cta, grid));
+        const int n = w.n_kv;
+        const int nr = next_round<KSPLIT>(p, round + 1, cta, grid);
+        WorkItem nw = w;
+        if (nr >= 0) nw = decode_item<KSPLIT>(p, item_of_round(nr, cta, grid));
+        if (first) {
+          // the first slot of the stream holds K_0 alone (position 1)
+          ok = load_q(0, w.hq0, w.r0, w.b) && load_slot(nullptr, 0, 0, 0, &tm_k, 0, w.kvh, w.b) &&
+               load_q(1, w.hq1, w.r1, w.b);
+          first = false;
+        } else {
+          ok = load_q(0, w.hq0, w.r0, w.b) && load_q(1, w.hq1, w.r1, w.b);
+        }
+        if (ok && nr >= 0) prefetch_q(nw);
+        for (int j = 0; ok && j < n; ++j) {
+          if (j + 1 < n)
+            ok = load_slot(&tm_v, j, w.kvh, w.b, &tm_k, j + 1, w.kvh, w.b);
+          else
+            ok = load_slot(&tm_v, j, w.kvh, w.b, nr >= 0 ? &tm_k : nullptr, 0, nw.kvh, nw.b);
+        }
+        ++act;
+        round = nr;
+      }
     }
     if (!ok && lane == 0) {
       // Let copies already in flight land before the CTA leaves: wait (bounded)
@@ -417,16 +455,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       return true;
     };
     if (lane == 0) {
-      for (int round = 0; ok; ++round) {
-        const int idx = item_of_round(round, cta, grid);
-        if (round * grid >= p.n_items) break;
-        if (idx >= p.n_items) continue;
-        const WorkItem w = decode_item<KSPLIT>(p, idx);
-        if (w.n_kv == 0) continue;
-        const int n = w.n_kv;
-        const uint32_t par = act & 1u;
-        uint32_t sl = 0;
-        if constexpr (KSPLIT) {
+      if constexpr (KSPLIT) {
+        for (int round = 0; ok; ++round) {
+          const int idx = item_of_round(round, cta, grid);
+          if (round * grid >= p.n_items) break;
+          if (idx >= p.n_items) continue;
+          const WorkItem w = decode_item<KSPLIT>(p, idx);
+          if (w.n_kv == 0) continue;
+          const int n = w.n_kv;
+          const uint32_t par = act & 1u;
+          uint32_t sl = 0;
           // Slot t runs key tiles t, t+2, ...: S_t from its first key tile,
           // then per step P_t V and the next S_t, each from a ring slot of its
           // own.
@@ -469,51 +507,81 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
           }
           ++act;
-          continue;
         }
-        // prologue: S_0 = Q_0 K_0^T as soon as Q_0 and K_0 land, then S_1
-        if (!(ok = bar_wait(bar_q_full, par, abort_flag, p) && wait_slot(sl))) break;
-        ptx::tc_fence_after();
-        issue_s(0, 2 * sl, 0, kS);
-        ptx::mma_commit(bar_s_full);
-        if (n == 1) ptx::mma_commit(bar_q_empty);
-        if (!(ok = bar_wait(bar_q_full + 8, par, abort_flag, p))) break;
-        ptx::tc_fence_after();
-        issue_s(1, 2 * sl, 0, kS);
-        ptx::mma_commit(bar_s_full + 8);
-        if (n == 1) ptx::mma_commit(bar_q_empty + 8);
-        bool seen[2] = {false, false};   // P_t's next phase already seen complete
-        for (int j = 0; ok && j < n; ++j) {
-          const bool more = (j + 1 < n);
-          const bool last_s = (j + 2 == n);   // S_t(j+1) is the item's last use of Q_t
-          // One slot holds V_j (position 0) and K_{j+1} (position 1). The MMA
-          // thread does not wait for it: the tile-0 softmax checks it before
-          // it signals P_0(j), so P_0 ready implies the slot is full, and the
-          // tile-1 softmax releases it.
-          sl = slot_it % kSlots;
-          ++slot_it;
-          for (int t = 0; t < 2; ++t) {
-            if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-            if (!(ok = wait_p(t, seen[t]))) break;
-            // the group: P_t V_j, then Q_t K_{j+1}^T; the next group's P is
-            // tested just before the group's last MMA
-            const int o = 1 - t;
-            if (more) {
-              issue_pv(t, 2 * sl, 0, kPV, j == 0);
-              issue_s(t, 2 * sl + 1, 0, kS - 1);
-              seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
-              issue_s(t, 2 * sl + 1, kS - 1, kS);
-              ptx::mma_commit(bar_s_full + 8 * t);
-              if (last_s) ptx::mma_commit(bar_q_empty + 8 * t);
-            } else {
-              issue_pv(t, 2 * sl, 0, kPV - 1, j == 0);
-              seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
-              issue_pv(t, 2 * sl, kPV - 1, kPV, false);
-              ptx::mma_commit(bar_o_full + 8 * t);
+      } else {
+        // Row-tile pairs, the CTA's items back to back (see the producer): the
+        // last group of an item issues, after P_t V_{n-1}, the next item's
+        // first S_t from K_0 in the same slot.
+        int round = next_round<KSPLIT>(p, 0, cta, grid);
+        if (round >= 0) {
+          int n = decode_item<KSPLIT>(p, item_of_round(round, cta, grid)).n_kv;
+          uint32_t sl = 0;
+          // prologue of the stream: S_0 = Q_0 K_0^T as soon as Q_0 and K_0
+          // (position 1 of the first slot) land, then S_1
+          ok = bar_wait(bar_q_full, 0, abort_flag, p) && wait_slot(sl);
+          if (ok) {
+            ptx::tc_fence_after();
+            issue_s(0, 2 * sl + 1, 0, kS);
+            ptx::mma_commit(bar_s_full);
+            if (n == 1) ptx::mma_commit(bar_q_empty);
+            ok = bar_wait(bar_q_full + 8, 0, abort_flag, p);
+          }
+          if (ok) {
+            ptx::tc_fence_after();
+            issue_s(1, 2 * sl + 1, 0, kS);
+            ptx::mma_commit(bar_s_full + 8);
+            if (n == 1) ptx::mma_commit(bar_q_empty + 8);
+          }
+          while (ok) {
+            const uint32_t par = act & 1u;
+            const int nr = next_round<KSPLIT>(p, round + 1, cta, grid);
+            const int nn = nr >= 0 ? decode_item<KSPLIT>(p, item_of_round(nr, cta, grid)).n_kv : 0;
+            bool seen[2] = {false, false};   // P_t's next phase already seen complete
+            for (int j = 0; ok && j < n; ++j) {
+              const bool more = (j + 1 < n);
+              const bool last_s = (j + 2 == n);   // S_t(j+1) is the item's last use of Q_t
+              // One slot holds V_j (position 0) and K_{j+1} (position 1), or
+              // after the last V the next item's K_0. The MMA thread does not
+              // wait for it: the tile-0 softmax checks it before it signals
+              // P_0(j), so P_0 ready implies the slot is full, and the tile-1
+              // softmax releases it.
+              sl = slot_it % kSlots;
+              ++slot_it;
+              for (int t = 0; t < 2; ++t) {
+                if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
+                if (!(ok = wait_p(t, seen[t]))) break;
+                // the group: P_t V_j, then Q_t K_{j+1}^T; the next group's P is
+                // tested just before the group's last MMA
+                const int o = 1 - t;
+                if (more) {
+                  issue_pv(t, 2 * sl, 0, kPV, j == 0);
+                  issue_s(t, 2 * sl + 1, 0, kS - 1);
+                  seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
+                  issue_s(t, 2 * sl + 1, kS - 1, kS);
+                  ptx::mma_commit(bar_s_full + 8 * t);
+                  if (last_s) ptx::mma_commit(bar_q_empty + 8 * t);
+                } else {
+                  issue_pv(t, 2 * sl, 0, kPV - 1, j == 0);
+                  seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
+                  issue_pv(t, 2 * sl, kPV - 1, kPV, false);
+                  ptx::mma_commit(bar_o_full + 8 * t);
+                  if (nr >= 0) {
+                    // the next item's S_t = Q_t K_0^T, K_0 at position 1
+                    if (!(ok = bar_wait(bar_q_full + 8 * t, par ^ 1u, abort_flag, p))) break;
+                    ptx::tc_fence_after();
+                    issue_s(t, 2 * sl + 1, 0, kS);
+                    ptx::mma_commit(bar_s_full + 8 * t);
+                    if (nn == 1) ptx::mma_commit(bar_q_empty + 8 * t);
+                  }
+                }
+              }
             }
+            ++act;
+            if (nr < 0) break;
+            round = nr;
+            n = nn;
           }
         }
-        ++act;
       }
       if (!ok) {
         // Wait (bounded) for every MMA already issued before TMEM is released.
@@ -535,7 +603,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int offset = p.Sk - p.Sq;
     uint32_t s_phase = 0, act = 0;
     // Row-tile pairs: K/V ring slot uses, counted like the producer's (an
-    // item of n key tiles uses n + 1 slots: K_0, then (V_j, K_{j+1})).
+    // item of n key tiles starts at the use that holds its K_0 and ends at
+    // use0 + n, which holds its last V and the next item's K_0).
     uint32_t slot_it = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -583,10 +652,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!(ok = bar_wait(bar_s_full + 8 * t, s_phase, abort_flag, p))) break;
         if constexpr (!KSPLIT) {
           // S_1(j) has completed, and with it every MMA that reads ring slot
-          // use j (K_0 when j = 0, else V_{j-1} and K_j): release the slot
+          // use0 + j (K_0 when j = 0, beside the previous item's last V;
+          // else V_{j-1} and K_j): release the slot
           if (warp == 4 && lane == 0) ptx::mbar_arrive(bar_kv_empty + 8 * ((use0 + j) % kSlots));
-          // The MMA thread reads V_j and K_{j+1} (slot use j + 1) as soon as
-          // it sees P_0(j), without a wait of its own: P_0(j) is signalled
+          // The MMA thread reads V_j and K_{j+1} (slot use0 + j + 1) as soon
+          // as it sees P_0(j), without a wait of its own: P_0(j) is signalled
           // only after this wait (normally long satisfied) has seen the slot
           // full.
           if (warp == 0) {
@@ -771,9 +841,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       // ---- epilogue: O = O~ / l, LSE = (m + log2 l) * ln 2
       if (!(ok = bar_wait(bar_o_full + 8 * t, act & 1u, abort_flag, p))) break;
-      // P_1 V_{n-1}, the last reader of slot use n, has completed: release it
-      if (t == 1 && warp == 4 && lane == 0) ptx::mbar_arrive(bar_kv_empty + 8 * ((use0 + w.n_kv) % kSlots));
-      slot_it = use0 + w.n_kv + 1;
+      // The item's last slot use (use0 + n) also holds the next item's K_0:
+      // the next item's tile-1 softmax releases it with its first S_1.
+      slot_it = use0 + w.n_kv;
       ptx::tc_fence_after();
       uint32_t orr[D];
       if constexpr (D == 128) {
