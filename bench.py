@@ -40,7 +40,8 @@ DEFAULT_WORKLOAD = "causal_gqa8_b1_s16384"
 L2_BYTES = 129 * 1000 * 1000
 DATASHEET_BF16_TFLOPS = 2250.0   # GB300 dense BF16/FP16 tensor peak (nominal, without 2:4 sparsity)
 METRIC = "attention fwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 tensor peak"
-KERNEL_SOURCES = ["exact_attention_16_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_16_gb300/csrc/ptx_sm103.cuh"]
+KERNEL_SOURCES = ["exact_attention_16_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_16_gb300/csrc/ptx_sm103.cuh",
+                  "exact_attention_16_gb300/csrc/softmax_row.cuh"]
 TRAFFIC_SUMMARY = "profiles/fa_fwd_kernel_traffic.md"
 
 
