@@ -198,14 +198,35 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
         ptx::tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, bar_q_full, c * 64, kvh * p.G, pos0, b + p.q_b_shift, pol_q);
-      // units in order K_0, V_0, K_1, V_1, ... (each in kHalves pieces)
+      // Tiles in the order the MMA thread consumes them (each in kHalves
+      // pieces): K_0, K_1, then V_0, K_2, V_1, K_3, ..., V_{n-2}, V_{n-1}
+      // (S runs two key tiles ahead of P V). Loading in this order, a ring
+      // unit is refilled with the next tile the MMA needs once the oldest one
+      // is consumed; K_{j+2} is not queued behind V_{j+1}.
       for (int u = 0; ok && u < 2 * kHalves * n; ++u) {
         const uint32_t st = u % kStages, ph = ((u / kStages) & 1u) ^ 1u;
         if (!(ok = dec_wait(bar_kv_empty + 8 * st, ph, abort_flag, p))) break;
         ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * st, L::kUnitBytes);
-        const int jt = u / (2 * kHalves), h = u % kHalves, key0 = (t_begin + jt) * 128;
+        const int pos = u / kHalves, h = u % kHalves;
+        const int lead = n < 2 ? n : 2;                   // K tiles before the first V
+        bool is_k;
+        int jt;
+        if (pos < lead) {
+          is_k = true;
+          jt = pos;
+        } else {
+          const int q = pos - 2;                          // -1 when n == 1
+          if (q < 2 * (n - 2)) {
+            is_k = (q & 1) != 0;
+            jt = is_k ? q / 2 + 2 : q / 2;
+          } else {
+            is_k = false;
+            jt = q - (n - 2);
+          }
+        }
+        const int key0 = (t_begin + jt) * 128;
         const uint32_t dst = sKV + st * L::kUnitBytes;
-        if ((u / kHalves) % 2 == 0) {
+        if (is_k) {
           // K: column chunks h * kChunks / kHalves ..., all 128 keys
 #pragma unroll
           for (int c = 0; c < L::kChunks / kHalves; ++c)
@@ -245,14 +266,17 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     constexpr int kPVU = 8 / kHalves;           // k-steps of P V (16 keys each) per V unit
     if (lane == 0 && n > 0) {
       bool ok = true;
-      auto wait_unit = [&](int u) -> bool {   // ring unit u (see the producer)
+      // Ring units are consumed in load order (see the producer): the issue
+      // sequence S_0, S_1, P V_0, S_2, P V_1, ... takes the next unit each time.
+      int next_u = 0;
+      auto wait_unit = [&](int u) -> bool {
         return dec_wait(bar_kv_full + 8 * (u % kStages), (u / kStages) & 1u, abort_flag, p);
       };
       // S buffer jt%2 = Q K_jt^T
       auto issue_s = [&](int jt) -> bool {
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
-          const int u = 2 * kHalves * jt + h;
+          const int u = next_u++;
           const uint32_t st = u % kStages;
           if (!wait_unit(u)) return false;
           ptx::tc_fence_after();
@@ -274,7 +298,7 @@ fa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (!(ok = dec_wait(bar_p_full, j & 1, abort_flag, p))) break;
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
-          const int u = 2 * kHalves * j + kHalves + h;
+          const int u = next_u++;
           const uint32_t vst = u % kStages;
           if (!(ok = wait_unit(u))) break;
           ptx::tc_fence_after();
