@@ -75,6 +75,28 @@ def test_full_size_workloads_every_element(w):
     check_every_element_pooled(w, out, lse, q, k, v)
 
 
+# More row-tile-pair items than a 152-SM grid has CTAs, so CTAs run items back
+# to back (each item's first Q K^T issued from the previous item's last K/V
+# slot). At D = 64 P has tensor-memory columns of its own and the next Q K^T
+# runs beside the softmax; at D = 128 P overwrites S.
+SEVERAL_ITEMS = [
+    W(1, 1280, 1280, 32, 16, 64, causal=True, seed=71),            # 160 items, causal lengths 1..10
+    W(2, 1000, 1100, 24, 6, 64, "fp16", causal=False, seed=72),    # 192 items, ragged row and key tails
+    W(1, 2560, 2800, 16, 16, 64, causal=True, sigma=2.0, seed=73),  # MHA: pairs of row tiles, offset mask
+    W(1, 1280, 1280, 32, 16, 128, causal=True, seed=74),
+]
+
+
+@pytest.mark.parametrize("w", SEVERAL_ITEMS, ids=["d64_causal_160", "d64_ragged_192", "d64_mha_offset",
+                                                  "d128_causal_160"])
+def test_row_tile_pairs_several_items_per_cta_every_element(w):
+    assert api.fa_debug_set_schedule(0) == api.FA_OK
+    try:
+        check_full(w)
+    finally:
+        api.fa_debug_set_schedule(-1)
+
+
 def test_sk_zero_gives_zero_output_and_neg_inf_lse():
     q = torch.randn(1, 5, 2, 128, dtype=torch.bfloat16, device="cuda")
     k = torch.empty(1, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
