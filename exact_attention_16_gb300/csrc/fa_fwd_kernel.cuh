@@ -86,7 +86,7 @@ struct Smem {
   static constexpr int kOStageWarpBytes = 32 * 128;
   static constexpr int kBarOff = kOStageOff + 8 * kOStageWarpBytes;
   // barriers: q_full[2] q_empty[2] kv_full[S/2] kv_empty[S/2] s_full[2]
-  //           p_full[2] (2 unused) o_full[2] o_empty[2] teardown stats_full
+  //           p_full[2] p_half[2] o_full[2] o_empty[2] teardown stats_full
   //           stats_empty (at most this many)
   static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 2 + 1 + 2;
   // Key-split items: slot 1 hands its per-row (m, l, l_corr) to the tile-0
@@ -200,6 +200,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   constexpr int kSlots = L::kStages / 2;   // K/V ring slots of two tiles each
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // Row-tile pairs at D = 64: the softmax signals the first half of P (keys
+  // 0..63) on its own, and the MMA thread starts P V on it while the second
+  // half is computed (the P V MMAs are short there; at D = 128 the extra
+  // hand-off cost more than the overlap gained).
+  constexpr bool kHalfP = !KSPLIT && D == 64;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -215,6 +220,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const uint32_t bar_kv_empty = bar_kv_full + kSlots * 8;  // [kSlots]
   const uint32_t bar_s_full = bar_kv_empty + kSlots * 8;   // [2]
   const uint32_t bar_p_full = bar_s_full + 2 * 8;          // [2] P (all 64 columns) written
+  const uint32_t bar_p_half = bar_p_full + 2 * 8;          // [2] row-tile pairs: P columns 0..31 written
   const uint32_t bar_o_full = bar_p_full + 4 * 8;          // [2]
   const uint32_t bar_o_empty = bar_o_full + 2 * 8;         // [2]
   const uint32_t bar_teardown = bar_o_empty + 2 * 8;
@@ -232,6 +238,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_init(bar_q_empty + 8 * t, 1);
       ptx::mbar_init(bar_s_full + 8 * t, 1);
       ptx::mbar_init(bar_p_full + 8 * t, 4);   // one arrival per softmax warp
+      ptx::mbar_init(bar_p_half + 8 * t, 4);
       ptx::mbar_init(bar_o_full + 8 * t, 1);
       ptx::mbar_init(bar_o_empty + 8 * t, 128);
     }
@@ -412,7 +419,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint64_t dq1 = ptx::sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
     const uint64_t dk0 = ptx::sdesc_sw128(sKV, 16, 1024);                 // K: K-major
     const uint64_t dv0 = ptx::sdesc_sw128(sKV, L::kChunkBytes, 1024);     // V: MN-major
-    uint32_t slot_it = 0, act = 0, p_phase[2] = {0u, 0u};
+    uint32_t slot_it = 0, act = 0, p_phase[2] = {0u, 0u}, ph_phase[2] = {0u, 0u};
     bool ok = true;
     // S_t = Q_t K^T with K in ring tile kt, k-steps [k0, k1).
     auto issue_s = [&](int t, uint32_t kt, int k0, int k1) {
@@ -451,6 +458,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     auto wait_p = [&](int t, bool seen) -> bool {
       if (!seen && !bar_wait(bar_p_full + 8 * t, p_phase[t], abort_flag, p)) return false;
       p_phase[t] ^= 1u;
+      ptx::tc_fence_after();
+      return true;
+    };
+    // Row-tile pairs: the first half of P_t (keys 0..63) ready.
+    auto wait_p_half = [&](int t, bool seen) -> bool {
+      if (!seen && !bar_wait(bar_p_half + 8 * t, ph_phase[t], abort_flag, p)) return false;
+      ph_phase[t] ^= 1u;
       ptx::tc_fence_after();
       return true;
     };
@@ -543,26 +557,35 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               // One slot holds V_j (position 0) and K_{j+1} (position 1), or
               // after the last V the next item's K_0. The MMA thread does not
               // wait for it: the tile-0 softmax checks it before it signals
-              // P_0(j), so P_0 ready implies the slot is full, and the tile-1
-              // softmax releases it.
+              // P_0(j) (at D = 64, its first half), so that signal implies the
+              // slot is full, and the tile-1 softmax releases it.
               sl = slot_it % kSlots;
               ++slot_it;
               for (int t = 0; t < 2; ++t) {
                 if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-                if (!(ok = wait_p(t, seen[t]))) break;
-                // the group: P_t V_j, then Q_t K_{j+1}^T; the next group's P is
+                // the group: P_t V_j (its first half as soon as the softmax
+                // has written keys 0..63 of P_t, while it computes the rest),
+                // then Q_t K_{j+1}^T; the next group's first half of P is
                 // tested just before the group's last MMA
+                const int kv0 = kHalfP ? kPV / 2 : 0;   // P V k-steps issued before all of P_t is in
+                if constexpr (kHalfP) {
+                  if (!(ok = wait_p_half(t, seen[t]))) break;
+                  issue_pv(t, 2 * sl, 0, kv0, j == 0);
+                }
+                if (!(ok = wait_p(t, kHalfP ? false : seen[t]))) break;
                 const int o = 1 - t;
+                const uint32_t next_p = kHalfP ? bar_p_half + 8 * o : bar_p_full + 8 * o;
+                const uint32_t next_ph = kHalfP ? ph_phase[o] : p_phase[o];
                 if (more) {
-                  issue_pv(t, 2 * sl, 0, kPV, j == 0);
+                  issue_pv(t, 2 * sl, kv0, kPV, kv0 == 0 && j == 0);
                   issue_s(t, 2 * sl + 1, 0, kS - 1);
-                  seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
+                  seen[o] = ptx::mbar_test_wait(next_p, next_ph);
                   issue_s(t, 2 * sl + 1, kS - 1, kS);
                   ptx::mma_commit(bar_s_full + 8 * t);
                   if (last_s) ptx::mma_commit(bar_q_empty + 8 * t);
                 } else {
-                  issue_pv(t, 2 * sl, 0, kPV - 1, j == 0);
-                  seen[o] = ptx::mbar_test_wait(bar_p_full + 8 * o, p_phase[o]);
+                  issue_pv(t, 2 * sl, kv0, kPV - 1, kv0 == 0 && j == 0);
+                  seen[o] = ptx::mbar_test_wait(next_p, next_ph);
                   issue_pv(t, 2 * sl, kPV - 1, kPV, false);
                   ptx::mma_commit(bar_o_full + 8 * t);
                   if (nr >= 0) {
@@ -656,9 +679,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           // else V_{j-1} and K_j): release the slot
           if (warp == 4 && lane == 0) ptx::mbar_arrive(bar_kv_empty + 8 * ((use0 + j) % kSlots));
           // The MMA thread reads V_j and K_{j+1} (slot use0 + j + 1) as soon
-          // as it sees P_0(j), without a wait of its own: P_0(j) is signalled
-          // only after this wait (normally long satisfied) has seen the slot
-          // full.
+          // as it sees P_0(j) (at D = 64, its first half), without a wait of
+          // its own: that is signalled only after this wait (normally long
+          // satisfied) has seen the slot full.
           if (warp == 0) {
             const uint32_t u = use0 + j + 1;
             bool r = true;
@@ -742,6 +765,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             ptx::tmem_st_32x32b_x32(tO + c * 32, orr);
           }
+        }
+        if constexpr (kHalfP) {
+          // keys 0..63 of P_t and any rescale of O~ are in tensor memory:
+          // the MMA thread may start P_t V_j on them
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar_p_half + 8 * t);
         }
         {
           uint32_t pk[32];
