@@ -310,6 +310,36 @@ def test_explicit_scales(scale):
 INT_LSE_MAX_ABS = 5e-5
 
 
+def _rising_scores(B, Sq, Sk, Hq, Hkv, D, seed=41):
+    """Scores that rise by about 10 (in log2 units) every 128 keys: q is all
+    ones and every component of key j is 0.054 j / sqrt(D), so with the
+    default scale s_ij = 0.054 j. Each key tile raises the row max past the
+    lazy-rescale threshold, so O~ is rescaled on every tile, and a rescale
+    that landed after P V had started, or was skipped, would leave earlier
+    tiles weighted 2^10 too high."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.ones(B, Sq, Hq, D).to(torch.bfloat16)
+    c = (0.054 * torch.arange(Sk, dtype=torch.float64) / D ** 0.5).to(torch.float32)
+    k = c.view(1, Sk, 1, 1).expand(B, Sk, Hkv, D).contiguous().to(torch.bfloat16)
+    v = torch.randn(B, Sk, Hkv, D, generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mode", [0, 1], ids=["pairs", "keysplit"])
+def test_rescale_on_every_key_tile(mode, D, causal):
+    q, k, v = _rising_scores(2, 300, 700, 4, 2, D)
+    assert api.fa_debug_set_schedule(mode) == api.FA_OK
+    try:
+        o, lse = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+        torch.cuda.synchronize()
+    finally:
+        api.fa_debug_set_schedule(-1)
+    assert api.fa_status() == 0
+    _oracle_compare(q, k, v, o, lse, D ** -0.5, causal)
+
+
 def _integer_inputs(B, Sq, Sk, Hq, Hkv, D, dtype, seed):
     """Integer-valued q, k, v in [-2, 2) (the integer test inputs of the
     CuTe-DSL example "ampere/flash_attention_v2.py", whose Q K^T is exact in
