@@ -563,10 +563,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               ++slot_it;
               for (int t = 0; t < 2; ++t) {
                 if (j == 0 && !(ok = bar_wait(bar_o_empty + 8 * t, par ^ 1u, abort_flag, p))) break;
-                // the group: P_t V_j (its first half as soon as the softmax
-                // has written keys 0..63 of P_t, while it computes the rest),
-                // then Q_t K_{j+1}^T; the next group's first half of P is
-                // tested just before the group's last MMA
+                // the group: P_t V_j (at D = 64 its first half as soon as the
+                // softmax has written keys 0..63 of P_t, while it computes the
+                // rest), then Q_t K_{j+1}^T; the next group's P (first half)
+                // is tested just before the group's last MMA
                 const int kv0 = kHalfP ? kPV / 2 : 0;   // P V k-steps issued before all of P_t is in
                 if constexpr (kHalfP) {
                   if (!(ok = wait_p_half(t, seen[t]))) break;
